@@ -1,0 +1,20 @@
+"""Persistent elementwise add oracle (test infrastructure only).
+
+helion "Implement persistent kernels", the ``_simple_add_kernel`` listings: every element of
+the result is ``x + y`` in the inputs' dtype (fp32); the persistent tile loop only decides
+which program writes which element, never the value.  numpy's float32 addition is the
+IEEE-754 binary32 sum with round-to-nearest-even and gradual underflow, which is the value
+every correct implementation must produce bit for bit.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def add_f32(x, y) -> np.ndarray:
+    x = np.asarray(x, dtype=np.float32)
+    y = np.asarray(y, dtype=np.float32)
+    if x.shape != y.shape:
+        raise ValueError("x and y must have the same shape")
+    with np.errstate(over="ignore", invalid="ignore"):
+        return np.add(x, y, dtype=np.float32)

@@ -1,0 +1,208 @@
+"""Tile-scheduler oracle: which output tiles each persistent worker visits, in order.
+
+Test infrastructure only.  A *worker* is one persistent CTA (1-CTA kernels) or one
+CTA pair (2-CTA clusters); ``P`` is the number of workers launched.  Tiles are
+numbered ``t in [0, T)``; the decode maps ``t`` to ``(m_idx, n_idx)`` where ``m_idx``
+counts cluster rows (``cs * BM`` rows of C each) and ``n_idx`` counts ``BN`` columns.
+For a CTA of rank ``cta_id`` inside its pair the tile row is ``bx = m_idx * cs + cta_id``.
+
+Orders (helion "Implement persistent kernels", persistent_blocked / persistent_interleaved
+kernels; tilelang "Introduce tile scheduler", the waves loop of the 2-CTA kernel):
+
+* blocked: worker p visits ``[p*B, min((p+1)*B, T))`` with ``B = ceil(T / P)``.
+* interleaved: worker p visits ``p, p+P, p+2P, ...``; the iteration index is the
+  tilelang "wave" ``w`` with ``tile_id = num_clusters * w + cluster_id``.
+
+Decodes:
+
+* linear (helion): ``m = t mod m_tiles``, ``n = t div m_tiles`` (rows vary fastest).
+* swizzled (tilelang, group of ``G`` column blocks): within a group of ``G*mc`` tiles the
+  column cycles fastest over the group's width, then the cluster row advances.  This is
+  the page's ``bx_cluster = (t // G) % mc``, ``by = t % G + (t // G) // mc * G`` whenever
+  ``n_blocks % G == 0``; a ragged last group takes the width ``n_blocks - g*G``
+  (reading: the page asserts divisibility instead).  ``mc = ceil(m_blocks / cs)``
+  (reading: the page floors it, which drops rows; the review on that kernel notes the
+  out-of-range ``bx`` this produces).
+* grouped-M (helion "PERSISTENT BLOCKED WITH L2 GROUPING"): bands of ``G`` tile rows,
+  rows fastest inside a band.
+
+Work stealing (tritonBLAS "Work Stealing Scheduler Kernel": per-XCD int32 tile counters
+indexed by ``pid % NUM_XCDS``, reset before each launch).  The fetch body is not on that
+page; the reading adopted here: ``G_ws`` counters; group ``g`` owns the contiguous tile
+range ``[floor(g*T/G_ws), floor((g+1)*T/G_ws))``; worker ``c`` starts at its home group
+``c mod G_ws``; a fetch is ``ticket = atomic_add(counter[g], 1)`` and succeeds when
+``ticket < size_g`` (tile ``start_g + ticket``); an exhausted group sends the worker on to
+``g+1, g+2, ...`` (mod ``G_ws``) and it stops once it has found all ``G_ws`` groups
+exhausted.  Stolen tiles are decoded with the swizzled decode (linear when ``G <= 1``).
+The visit order is not deterministic, so only the properties in :func:`check_ws_trace`
+are fixed.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+BLOCKED, INTERLEAVED, SWIZZLED, WORK_STEALING, BLOCKED_GROUPED_M = 0, 1, 2, 3, 4
+MODE_NAMES = {
+    BLOCKED: "blocked",
+    INTERLEAVED: "interleaved",
+    SWIZZLED: "swizzled",
+    WORK_STEALING: "work_stealing",
+    BLOCKED_GROUPED_M: "blocked_grouped_m",
+}
+
+
+def cdiv(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+@dataclass(frozen=True)
+class Grid:
+    """Tile-grid geometry for C (M x N) cut into (cs*BM) x BN cluster tiles."""
+
+    m_blocks: int  # CTA tile rows: ceil(M / BM)
+    n_blocks: int  # tile columns: ceil(N / BN)
+    cs: int  # CTAs per cluster along M (1 or 2)
+
+    @property
+    def m_clusters(self) -> int:
+        return cdiv(self.m_blocks, self.cs)
+
+    @property
+    def tiles(self) -> int:
+        return self.m_clusters * self.n_blocks
+
+
+def grid_for(M: int, N: int, BM: int, BN: int, cs: int = 1) -> Grid:
+    return Grid(cdiv(M, BM), cdiv(N, BN), cs)
+
+
+# ----------------------------------------------------------------------------- decodes
+def decode_linear(t: int, m_tiles: int) -> tuple[int, int]:
+    return t % m_tiles, t // m_tiles
+
+
+def decode_swizzled(t: int, G: int, mc: int, n_blocks: int) -> tuple[int, int]:
+    """Tile id -> (cluster row, column) with column groups of width G."""
+    span = G * mc
+    g, r = divmod(t, span)
+    gw = min(G, n_blocks - g * G)
+    return r // gw, g * G + r % gw
+
+
+def decode_grouped_m(t: int, G: int, m_tiles: int, n_tiles: int) -> tuple[int, int]:
+    per_group = G * n_tiles
+    group_id = t // per_group
+    first_m = group_id * G
+    gsm = min(m_tiles - first_m, G)
+    local = t % per_group
+    return first_m + local % gsm, local // gsm
+
+
+def decode(mode: int, t: int, grid: Grid, G: int) -> tuple[int, int]:
+    mc, nb = grid.m_clusters, grid.n_blocks
+    if mode in (BLOCKED, INTERLEAVED):
+        return decode_linear(t, mc)
+    if mode == BLOCKED_GROUPED_M:
+        return decode_grouped_m(t, max(G, 1), mc, nb)
+    if mode in (SWIZZLED, WORK_STEALING):
+        if G <= 1:
+            return decode_linear(t, mc)
+        return decode_swizzled(t, G, mc, nb)
+    raise ValueError(f"unknown mode {mode}")
+
+
+# ------------------------------------------------------------------------------ orders
+def order_blocked(T: int, P: int) -> list[list[int]]:
+    B = cdiv(T, P) if T else 0
+    return [list(range(p * B, min((p + 1) * B, T))) for p in range(P)]
+
+
+def order_interleaved(T: int, P: int) -> list[list[int]]:
+    return [list(range(p, T, P)) for p in range(P)]
+
+
+def static_schedule(mode: int, grid: Grid, P: int, G: int) -> list[list[tuple[int, int, int, int]]]:
+    """Per worker, the ordered visits ``(iter, tile_id, m_idx, n_idx)`` of a static mode."""
+    T = grid.tiles
+    if mode in (BLOCKED, BLOCKED_GROUPED_M):
+        orders = order_blocked(T, P)
+    elif mode in (INTERLEAVED, SWIZZLED):
+        orders = order_interleaved(T, P)
+    else:
+        raise ValueError("work stealing has no static schedule; use ws_simulate")
+    out = []
+    for tiles in orders:
+        out.append([(i, t, *decode(mode, t, grid, G)) for i, t in enumerate(tiles)])
+    return out
+
+
+# ------------------------------------------------------------------------ work stealing
+def ws_partition(T: int, groups: int) -> list[tuple[int, int]]:
+    """(start, size) of each counter group's contiguous tile range."""
+    bounds = [(g * T) // groups for g in range(groups + 1)]
+    return [(bounds[g], bounds[g + 1] - bounds[g]) for g in range(groups)]
+
+
+class WsState:
+    """Counters plus each worker's cursor: the sequential model of the ticket protocol."""
+
+    def __init__(self, T: int, P: int, groups: int):
+        self.T, self.P, self.groups = T, P, groups
+        self.part = ws_partition(T, groups)
+        self.counter = [0] * groups
+        self.cursor = [0] * P  # groups already found exhausted, counted from home
+        self.done = [False] * P
+
+    def fetch(self, c: int) -> int:
+        """One fetch by worker c; returns a tile id or -1 once every group is exhausted."""
+        home = c % self.groups
+        while self.cursor[c] < self.groups:
+            g = (home + self.cursor[c]) % self.groups
+            ticket = self.counter[g]
+            self.counter[g] += 1  # the atomic add
+            start, size = self.part[g]
+            if ticket < size:
+                return start + ticket
+            self.cursor[c] += 1
+        self.done[c] = True
+        return -1
+
+
+def ws_simulate(T: int, P: int, groups: int, pick) -> list[list[int]]:
+    """Run the protocol with workers fetching in the order chosen by ``pick(live) -> c``."""
+    st = WsState(T, P, groups)
+    visits: list[list[int]] = [[] for _ in range(P)]
+    live = list(range(P))
+    while live:
+        c = pick(live)
+        t = st.fetch(c)
+        if t < 0:
+            live.remove(c)
+        else:
+            visits[c].append(t)
+    return visits
+
+
+def check_ws_trace(visits: list[list[int]], T: int, groups: int) -> None:
+    """Validate a work-stealing visit log (per worker, tile ids in visit order).
+
+    Raises AssertionError unless: every tile in [0, T) is visited exactly once; inside each
+    counter group a worker's tickets increase; and a worker's groups follow its cyclic
+    order from home (home, home+1, ...), never going back to a group it left.
+    """
+    flat = sorted(t for v in visits for t in v)
+    assert flat == list(range(T)), "work-stealing visits are not a permutation of the tiles"
+    part = ws_partition(T, groups)
+    owner = {}
+    for g, (s, n) in enumerate(part):
+        for t in range(s, s + n):
+            owner[t] = g
+    for c, v in enumerate(visits):
+        home = c % groups
+        last_off, last_t = -1, -1
+        for t in v:
+            off = (owner[t] - home) % groups
+            assert off >= last_off, f"worker {c} went back to an earlier group"
+            if off == last_off:
+                assert t > last_t, f"worker {c} tickets not increasing in group {owner[t]}"
+            last_off, last_t = off, t

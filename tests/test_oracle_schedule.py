@@ -1,0 +1,239 @@
+"""Pins for oracle.schedule: hand-evaluated page fixtures, the pages' literal formulas,
+brute-force bijection checks and planted mistakes in the work-stealing validator."""
+import itertools
+import random
+import threading
+
+import pytest
+
+from oracle import schedule as S
+
+
+# --------------------------------------------------------------- the pages' formulas, literal
+def helion_blocked(total, nsm, pid):
+    block_size = -(-total // nsm)
+    start = pid * block_size
+    end = min(start + block_size, total)
+    return list(range(start, end))
+
+
+def helion_interleaved(total, nsm, pid):
+    return list(range(pid, total, nsm))
+
+
+def helion_l2_group(vpid, num_pid_m, num_pid_n, group=8):
+    num_pid_in_group = group * num_pid_n
+    group_id = vpid // num_pid_in_group
+    first_pid_m = group_id * group
+    group_size_m = min(num_pid_m - first_pid_m, group)
+    pid_0 = first_pid_m + vpid % num_pid_in_group % group_size_m
+    pid_1 = vpid % num_pid_in_group // group_size_m
+    return pid_0, pid_1
+
+
+def tilelang_swizzle(tile_id, group_size, m_clusters):
+    bx_cluster = (tile_id // group_size) % m_clusters
+    by = (tile_id % group_size) + (tile_id // group_size) // m_clusters * group_size
+    return bx_cluster, by
+
+
+# ------------------------------------------------------------------------- golden fixtures
+def test_golden_helion_blocked(golden):
+    grid = S.grid_for(64, 48, 32, 16)
+    sched = S.static_schedule(S.BLOCKED, grid, 4, 1)
+    rows = [(p, i, t, m, n) for p, v in enumerate(sched) for (i, t, m, n) in v]
+    assert rows == golden("helion_persistent_blocked_64x48.txt")
+
+
+def test_golden_helion_interleaved(golden):
+    grid = S.grid_for(64, 48, 32, 16)
+    sched = S.static_schedule(S.INTERLEAVED, grid, 4, 1)
+    rows = [(p, i, t, m, n) for p, v in enumerate(sched) for (i, t, m, n) in v]
+    assert rows == golden("helion_persistent_interleaved_64x48.txt")
+
+
+def test_golden_helion_l2_grouping(golden):
+    grid = S.grid_for(320, 32, 32, 16)
+    sched = S.static_schedule(S.BLOCKED_GROUPED_M, grid, 8, 8)
+    rows = [(p, i, t, m, n) for p, v in enumerate(sched) for (i, t, m, n) in v]
+    assert rows == golden("helion_blocked_l2_grouping_320x32.txt")
+
+
+def test_golden_tilelang_swizzle(golden):
+    grid = S.grid_for(512, 512, 128, 128, cs=2)
+    sched = S.static_schedule(S.SWIZZLED, grid, 2, 2)  # 2 clusters = 4 CTAs
+    rows = []
+    for block_id in range(4):
+        cluster, cta = divmod(block_id, 2)
+        for (w, t, mi, n) in sched[cluster]:
+            rows.append((block_id, w, t, mi * 2 + cta, n))
+    assert sorted(rows) == sorted(golden("tilelang_swizzle_2cta_512x512.txt"))
+
+
+# ----------------------------------------------------------------- literal formulas, brute
+@pytest.mark.parametrize("T,P", [(t, p) for t in range(0, 40) for p in (1, 2, 3, 5, 8, 13)])
+def test_blocked_and_interleaved_match_helion(T, P):
+    assert S.order_blocked(T, P) == [helion_blocked(T, P, p) for p in range(P)]
+    assert S.order_interleaved(T, P) == [helion_interleaved(T, P, p) for p in range(P)]
+
+
+@pytest.mark.parametrize("mt,nt,G", list(itertools.product(range(1, 12), range(1, 7), (1, 2, 3, 8))))
+def test_grouped_m_matches_helion(mt, nt, G):
+    for t in range(mt * nt):
+        assert S.decode_grouped_m(t, G, mt, nt) == helion_l2_group(t, mt, nt, G)
+
+
+@pytest.mark.parametrize("mc,G,ngroups", list(itertools.product(range(1, 7), (1, 2, 3, 4, 16), (1, 2, 3))))
+def test_swizzle_matches_tilelang_when_divisible(mc, G, ngroups):
+    nb = G * ngroups
+    for t in range(mc * nb):
+        assert S.decode_swizzled(t, G, mc, nb) == tilelang_swizzle(t, G, mc)
+
+
+# ----------------------------------------------------------------------------- invariants
+MODES = [S.BLOCKED, S.INTERLEAVED, S.SWIZZLED, S.BLOCKED_GROUPED_M]
+
+
+@pytest.mark.parametrize("mb,nb,cs,G,P", [
+    (mb, nb, cs, G, P)
+    for mb in (1, 2, 3, 5, 6) for nb in (1, 2, 4, 5) for cs in (1, 2) for G in (1, 2, 3, 4) for P in (1, 3, 4, 8)
+])
+def test_every_tile_visited_exactly_once(mb, nb, cs, G, P):
+    grid = S.Grid(mb, nb, cs)
+    cells = {(m, n) for m in range(grid.m_clusters) for n in range(nb)}
+    for mode in MODES:
+        sched = S.static_schedule(mode, grid, P, G)
+        seen = [(m, n) for v in sched for (_, _, m, n) in v]
+        assert len(seen) == grid.tiles and set(seen) == cells, S.MODE_NAMES[mode]
+        ids = sorted(t for v in sched for (_, t, _, _) in v)
+        assert ids == list(range(grid.tiles))
+        for v in sched:
+            assert [i for (i, _, _, _) in v] == list(range(len(v)))
+
+
+def test_blocked_contiguous_and_interleaved_stride():
+    grid = S.Grid(19, 32, 1)  # 608 tiles, the (4864, 4096) ragged case with 256 x 128 tiles
+    P = 152
+    blk = S.static_schedule(S.BLOCKED, grid, P, 1)
+    assert all(v[-1][1] - v[0][1] == len(v) - 1 for v in blk if v)
+    assert sum(1 for v in blk if v) == 152 and {len(v) for v in blk} == {4}
+    inter = S.static_schedule(S.INTERLEAVED, grid, P, 1)
+    assert all(b[1] - a[1] == P for v in inter for a, b in zip(v, v[1:]))
+
+
+def test_blocked_idle_workers_when_tiles_do_not_divide():
+    # T = 608 tiles, P = 160 workers: ceil(608/160) = 4, so only 152 workers get work
+    blk = S.order_blocked(608, 160)
+    assert sum(1 for v in blk if v) == 152
+
+
+def test_decode_reductions():
+    for mc, nb in itertools.product(range(1, 9), range(1, 9)):
+        for t in range(mc * nb):
+            assert S.decode_swizzled(t, 1, mc, nb) == S.decode_linear(t, mc)
+            assert S.decode_grouped_m(t, mc, mc, nb) == S.decode_linear(t, mc)
+            r, c = divmod(t, nb)  # one group spanning all columns: columns fastest
+            assert S.decode_swizzled(t, nb, mc, nb) == (r, c)
+
+
+def test_ragged_last_swizzle_group_is_a_bijection():
+    for mc, nb, G in itertools.product(range(1, 8), range(1, 20), (2, 3, 4, 16)):
+        cells = [S.decode_swizzled(t, G, mc, nb) for t in range(mc * nb)]
+        assert sorted(cells) == [(m, n) for m in range(mc) for n in range(nb)]
+
+
+# -------------------------------------------------------------------------- work stealing
+def test_ws_partition_covers_tiles():
+    for T, G in itertools.product(range(0, 50), (1, 2, 3, 8)):
+        part = S.ws_partition(T, G)
+        ids = [t for (s, n) in part for t in range(s, s + n)]
+        assert ids == list(range(T))
+        sizes = [n for (_, n) in part]
+        assert max(sizes) - min(sizes) <= 1
+
+
+def test_ws_single_group_round_robin_is_interleaved():
+    T, P = 37, 5
+    order = itertools.cycle(range(P))
+    visits = S.ws_simulate(T, P, 1, lambda live: next(c for c in order if c in live))
+    assert visits == S.order_interleaved(T, P)
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_ws_random_interleavings_valid(seed):
+    rnd = random.Random(seed)
+    T, P, G = rnd.randint(0, 300), rnd.randint(1, 20), rnd.choice([1, 2, 3, 8])
+    visits = S.ws_simulate(T, P, G, lambda live: rnd.choice(live))
+    S.check_ws_trace(visits, T, G)
+
+
+def test_ws_threads_with_atomic_counters_valid():
+    T, P, G = 500, 12, 8
+    st = S.WsState(T, P, G)
+    lock = threading.Lock()
+    visits = [[] for _ in range(P)]
+
+    class AtomicState(S.WsState):
+        pass
+
+    def fetch(c):
+        home = c % G
+        while st.cursor[c] < G:
+            g = (home + st.cursor[c]) % G
+            with lock:  # the atomic add
+                ticket = st.counter[g]
+                st.counter[g] += 1
+            s0, n = st.part[g]
+            if ticket < n:
+                return s0 + ticket
+            st.cursor[c] += 1
+        return -1
+
+    def worker(c):
+        while True:
+            t = fetch(c)
+            if t < 0:
+                return
+            visits[c].append(t)
+
+    th = [threading.Thread(target=worker, args=(c,)) for c in range(P)]
+    for t in th:
+        t.start()
+    for t in th:
+        t.join()
+    S.check_ws_trace(visits, T, G)
+    # every counter ends at or above its group size (exhausted), never below
+    assert all(st.counter[g] >= n for g, (_, n) in enumerate(st.part))
+
+
+def _valid_trace():
+    rnd = random.Random(3)
+    return S.ws_simulate(60, 6, 3, lambda live: rnd.choice(live))
+
+
+@pytest.mark.parametrize("plant", ["dup", "drop", "swap", "back"])
+def test_ws_checker_rejects_planted_mistakes(plant):
+    visits = [list(v) for v in _valid_trace()]
+    c = max(range(len(visits)), key=lambda i: len(visits[i]))
+    if plant == "dup":
+        visits[c].append(visits[c][0])
+    elif plant == "drop":
+        visits[c].pop()
+    elif plant == "swap":
+        visits[c][0], visits[c][1] = visits[c][1], visits[c][0]
+    elif plant == "back":
+        # worker 0 (home group 0) visiting a group-2 tile before a group-0 tile
+        part = S.ws_partition(60, 3)
+        t_g2 = part[2][0]
+        for v in visits:
+            if t_g2 in v:
+                v.remove(t_g2)
+        visits[0].insert(0, t_g2)
+        if not any(part[0][0] <= t < part[0][0] + part[0][1] for t in visits[0][1:]):
+            t_g0 = part[0][0]
+            for v in visits:
+                if t_g0 in v:
+                    v.remove(t_g0)
+            visits[0].append(t_g0)
+    with pytest.raises(AssertionError):
+        S.check_ws_trace(visits, 60, 3)
