@@ -138,3 +138,16 @@ def add_inputs(rows: int, cols: int, seed: int):
     x = rng.standard_normal(size=(rows, cols)).astype(np.float32)
     y = rng.standard_normal(size=(rows, cols)).astype(np.float32)
     return x, y
+
+
+def gemm_bf16_sequence(shapes, seed: int, dist: str = "uniform"):
+    """Several bf16 GEMM operand pairs drawn from ONE seeded stream, in the order given:
+    A_0, B_0 (K x N), A_1, B_1, ...  Returns a list of (A_bits, B_bits)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for (M, N, K) in shapes:
+        scale = 1.0 / np.sqrt(K) if dist == "normal" else 1.0
+        a = f64_to_bf16_bits(_draw(rng, dist, (M, K), scale))
+        b = f64_to_bf16_bits(_draw(rng, dist, (K, N), scale))
+        out.append((a, b))
+    return out
