@@ -1,0 +1,362 @@
+"""Benchmark of the persistent tiled GEMM and the persistent add on GB300.
+
+Headline (``value``): bf16 GEMM C = A . B at M = N = K = 8192 (A, B ~ N(0,1)/sqrt(K), seed 2,
+B stored K x N), swizzled scheduler with group_size 16, in TFLOP/s over the whole job.
+One step = one GEMM launch through the C ABI.  The same run also reports, outside the
+timed headline loop: TFLOP/s per scheduler mode, the persistent add's GB/s on fp32
+8192 x 8192 (seed 1), tail idle per scheduler from traced launches, the end-to-end figure
+from host memory, and the CPU oracle timed on a bounded sample.
+
+``--impl reference`` times the CPU oracle (the reference arm of this build) on the same
+workload and prints the same JSON line with ``"impl": "reference"``.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+M = N = K = 8192
+FLOP = 2.0 * M * N * K
+ADD_ROWS = ADD_COLS = 8192
+ADD_BYTES = 12.0 * ADD_ROWS * ADD_COLS  # read x, read y, write out (fp32)
+METRIC = "GEMM TFLOP/s & % tensor peak per scheduler mode; persistent add GB/s vs HBM"
+WORKLOAD = "bf16 GEMM M=N=K=8192, A,B ~ N(0,1)/sqrt(K) seed 2, B stored KxN, swizzled group_size=16"
+L2_NOTE = "inputs larger than L2: A+B+C = 384 MiB per GEMM > 129 MB L2; add x+y+out = 768 MiB"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cfg", type=int, default=0, help="kernel configuration (PGT_CFG_*), 0 = auto")
+    ap.add_argument("--ragged", action="store_true", help="also measure the ragged-tail GEMM set")
+    ap.add_argument("--no-extras", action="store_true", help="headline only")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_burst": p["bf16_tflops"],
+                "bf16_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_burst": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons around a timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.15)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg, torch=None):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, value: float, device) -> float:
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- helpers
+def time_launches(torch, launch, steps: int, warmup: int):
+    """Run `warmup` untimed launches, then `steps` launches bracketed by CUDA events on the
+    current stream; returns (total ms, list of per-launch ms)."""
+    for _ in range(warmup):
+        launch()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    evs[0].record()
+    for i in range(steps):
+        launch()
+        evs[i + 1].record()
+    torch.cuda.synchronize()
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+    return evs[0].elapsed_time(evs[-1]), per
+
+
+def tail_idle(times_ns: np.ndarray) -> float:
+    """1 - sum(busy) / (P * span): the share of worker time spent idle in the launch."""
+    t = times_ns[(times_ns[:, 0] > 0) & (times_ns[:, 1] > 0)]
+    if len(t) == 0:
+        return float("nan")
+    span = float(t[:, 1].max() - t[:, 0].min())
+    return 1.0 - float((t[:, 1] - t[:, 0]).sum()) / (len(times_ns) * span) if span > 0 else 0.0
+
+
+def cpu_baseline(budget_s: float, A_bits, B_bits, rows_hint: int | None = None) -> dict:
+    """The CPU oracle, as it stands, on a bounded sample of rows of the same GEMM."""
+    from oracle import gemm as OG
+    cores = OG.num_threads()
+    B64 = OG.dequant_bf16(B_bits)
+    probe_rows = max(1, cores)
+    A64 = OG.dequant_bf16(A_bits[:probe_rows])
+    t0 = time.perf_counter()
+    OG.gemm_rows(A64, B64, True, K, N, np.arange(probe_rows))
+    t_probe = time.perf_counter() - t0
+    rows = rows_hint or int(max(probe_rows, min(M, probe_rows * budget_s / max(t_probe, 1e-3))))
+    rows = (rows // probe_rows) * probe_rows or probe_rows
+    A64 = OG.dequant_bf16(A_bits[:rows])
+    t0 = time.perf_counter()
+    OG.gemm_rows(A64, B64, True, K, N, np.arange(rows))
+    dt = time.perf_counter() - t0
+    return {"value": 2.0 * rows * N * K / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {rows} rows of C for the 8192^3 bf16 GEMM (fp64 C loops, OpenMP over rows), "
+                      f"{dt:.1f} s; operand decode not timed"}
+
+
+# ----------------------------------------------------------------- reference arm
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import synthetic
+    from oracle import gemm as OG
+    A, B = synthetic.gemm_bf16_inputs(M, N, K, seed=2, dist="normal")
+    cores = OG.num_threads()
+    B64 = OG.dequant_bf16(B)
+    rows = max(1, cores)
+    A64 = OG.dequant_bf16(A[:rows])
+    t0 = time.perf_counter()
+    OG.gemm_rows(A64, B64, True, K, N, np.arange(rows))
+    t_step = time.perf_counter() - t0
+    total_budget = 150.0
+    while rows > 1 and t_step * (args.steps + args.warmup) > total_budget:
+        rows //= 2
+        t_step /= 2
+    A64 = OG.dequant_bf16(A[:rows])
+    sel = np.arange(rows)
+    for _ in range(args.warmup):
+        OG.gemm_rows(A64, B64, True, K, N, sel)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        OG.gemm_rows(A64, B64, True, K, N, sel)
+    dt = time.perf_counter() - t0
+    val = 2.0 * rows * N * K * args.steps / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows} rows of C per step of the 8192^3 bf16 GEMM, fp64 oracle"},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------ our arm
+def run_ours(args, world, rank, local, pg):
+    import torch
+
+    import persistent_gemm_tile_gb300 as pgt
+    import synthetic
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    peaks = load_peaks()
+    ctx = pgt.Context(local, max_groups=16)
+    A, B = synthetic.gemm_bf16_inputs(M, N, K, seed=2, dist="normal")
+    dA = torch.from_numpy(A.view(np.int16)).to(device)
+    dB = torch.from_numpy(B.view(np.int16)).to(device)
+    dC = torch.empty((M, N), dtype=torch.int16, device=device)
+
+    def desc_for(mode, cfg=args.cfg):
+        return pgt.make_desc(M, N, K, b_layout=pgt.B_KN, sched_mode=mode, group_size=16, ws_groups=8,
+                             kernel_cfg=cfg)
+
+    head = desc_for(pgt.SWIZZLED)
+    plan = ctx.gemm_plan(head)
+    launch = lambda: ctx.gemm_ex(head, dA, dB, dC)  # noqa: E731
+
+    # ------------------------------------------------------------------ headline
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize()
+    barrier(pg)
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    clocks.start()
+    total_ms, per = time_launches(torch, launch, args.steps, 0)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(pg)
+    rc, detail = ctx.last_error()
+    if rc != 0:
+        raise RuntimeError(f"device-side timeout during the timed region: {detail}")
+    total_ms = max_over_ranks(pg, total_ms, device)
+    ms_per_step = total_ms / args.steps
+    value = world * FLOP * args.steps / (total_ms * 1e-3) / 1e12
+    kern_ms = float(np.mean(per))
+    achieved = FLOP / (kern_ms * 1e-3) / 1e12
+    long_region = total_ms > 500.0
+    peak = peaks["bf16_sustained"] if long_region else peaks["bf16_burst"]
+    out = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "kernel_cfg": plan["kernel_cfg"], "tile": f"{plan['bm']}x{plan['bn']}",
+                   "ctas_per_worker": plan["cluster_size"], "workers": plan["workers"], "stages": plan["stages"],
+                   "l2": L2_NOTE, "parallelism": f"{world} independent GEMMs (one per GPU)"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "peak_kind": ("sustained" if long_region else "burst") + f" bf16 ({peaks['source']})"},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    if rank != 0:
+        return
+    if not args.no_extras:
+        extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out)
+    print(json.dumps(out), flush=True)
+    ctx.close()
+
+
+def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
+    import synthetic
+    A_host = dA.cpu().numpy().view(np.uint16)
+    B_host = dB.cpu().numpy().view(np.uint16)
+    # per scheduler mode
+    per_mode = {}
+    names = {pgt.BLOCKED: "blocked", pgt.INTERLEAVED: "interleaved", pgt.SWIZZLED: "swizzled",
+             pgt.WORK_STEALING: "work_stealing", pgt.BLOCKED_GROUPED_M: "blocked_grouped_m"}
+    for mode, name in names.items():
+        d = desc_for(mode)
+        _, per = time_launches(torch, lambda: ctx.gemm_ex(d, dA, dB, dC), 40, 5)
+        ms = float(np.median(per))
+        tf = FLOP / (ms * 1e-3) / 1e12
+        per_mode[name] = {"tflops": tf, "ms": ms, "frac_of_burst_peak": tf / peaks["bf16_burst"]}
+    out["per_mode"] = per_mode
+    # tail idle from traced launches (not timed)
+    tails = {}
+    for mode, name in names.items():
+        d = desc_for(mode)
+        plan = ctx.gemm_plan(d)
+        tb = pgt.TraceBuffers(plan["ctas"], plan["tiles"], device=device)
+        ctx.gemm_ex(d, dA, dB, dC, trace=tb.struct)
+        torch.cuda.synchronize()
+        tails[name] = tail_idle(tb.times.cpu().numpy())
+    out["tail_idle"] = {"workload": "8192^3 bf16", **tails}
+    # persistent add
+    x, y = synthetic.add_inputs(ADD_ROWS, ADD_COLS, seed=1)
+    tx, ty = torch.from_numpy(x).to(device), torch.from_numpy(y).to(device)
+    to = torch.empty_like(tx)
+    add = {}
+    best = None
+    for tile, tname in (((0, 0), "wide_8x1024"), ((32, 16), "page_32x16")):
+        for mode, mname in ((pgt.BLOCKED, "blocked"), (pgt.INTERLEAVED, "interleaved")):
+            fn = lambda: ctx.add(tx, ty, to, sched_mode=mode, tile_r=tile[0], tile_c=tile[1])  # noqa: E731
+            _, per = time_launches(torch, fn, 30, 3)
+            ms = float(np.median(per))
+            gbs = ADD_BYTES / (ms * 1e-3) / 1e9
+            add[f"{tname}_{mname}"] = {"gbs": gbs, "ms": ms}
+            if best is None or gbs > best[1]:
+                best = (f"{tname}_{mname}", gbs, ms)
+    add["roofline"] = {"bound": "hbm", "achieved": best[1], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                       "frac": best[1] / peaks["hbm_gbs"], "traffic": None, "kernel": best[0],
+                       "algorithmic_bytes": ADD_BYTES}
+    add["workload"] = "fp32 8192x8192 x,y ~ N(0,1) seed 1, out = x + y"
+    out["add"] = add
+    del tx, ty, to
+    # end to end from pinned host memory through pgt_gemm_host
+    hA = torch.from_numpy(A_host.view(np.int16)).pin_memory()
+    hB = torch.from_numpy(B_host.view(np.int16)).pin_memory()
+    hC = torch.empty((M, N), dtype=torch.int16).pin_memory()
+    d = desc_for(pgt.SWIZZLED)
+    e2e_steps = max(3, min(args.steps, 20))
+    total, _ = time_launches(torch, lambda: ctx.gemm_host(d, hA, hB, hC, dA, dB, dC), e2e_steps, 2)
+    out["e2e"] = {"value": FLOP * e2e_steps / (total * 1e-3) / 1e12, "unit": "TFLOP/s",
+                  "h2d_bytes_per_step": int(hA.numel() * 2 + hB.numel() * 2),
+                  "d2h_bytes_per_step": int(hC.numel() * 2), "steps": e2e_steps}
+    # the oracle on the host cores
+    out["cpu_baseline"] = cpu_baseline(args.cpu_seconds, A_host, B_host)
+
+
+def main():
+    args = parse()
+    world, rank, local, pg = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local, pg)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

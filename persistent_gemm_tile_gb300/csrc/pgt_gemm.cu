@@ -46,11 +46,16 @@ struct Bf16Layout {
     static constexpr int BAR_OFF = EPI_OFF + kEpiWarps * 2 * kEpiBufBytes;
     // barriers: full[S], empty[S], tfull[2], tempty[2], sfull[Q], sempty[Q], mma_done
     static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * kTileRing + 1;
-    static constexpr int RING_OFF = BAR_OFF + NUM_BARS * 8;
+    // the ring holds int4 entries: 16-byte aligned
+    static constexpr int RING_OFF = BAR_OFF + (NUM_BARS * 8 + 15) / 16 * 16;
     static constexpr int MISC_OFF = RING_OFF + kTileRing * 16;  // tmem slot, abort flag
     static constexpr int BYTES = MISC_OFF + 16;
     static constexpr int SMEM = BYTES + 1024;  // alignment slack
     static constexpr int TMEM_COLS = 2 * BN;
+    static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
+    static_assert(EPI_OFF % 1024 == 0 && BAR_OFF % 1024 == 0, "epilogue buffers need 1024-byte alignment");
+    static_assert(RING_OFF % 16 == 0 && MISC_OFF % 16 == 0, "ring entries are 16-byte vectors");
+    static_assert(SMEM <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {

@@ -66,10 +66,11 @@ __device__ __forceinline__ void decode_grouped_m(int t, int G, int m_tiles, int 
 }
 
 __device__ __forceinline__ void decode_tile(const SchedParams& p, int t, int& m, int& n) {
-    if (p.mode == kBlocked || p.mode == kInterleaved || p.group <= 1) {
-        decode_linear(t, p.m_tiles, m, n);
-    } else if (p.mode == kBlockedGroupedM) {
+    if (p.mode == kBlockedGroupedM) {
+        // the L2-grouping formula for every group width (width 1 gives columns fastest)
         decode_grouped_m(t, p.group, p.m_tiles, p.n_tiles, m, n);
+    } else if (p.mode == kBlocked || p.mode == kInterleaved || p.group <= 1) {
+        decode_linear(t, p.m_tiles, m, n);
     } else {
         decode_swizzled(t, p.group, p.m_tiles, p.n_tiles, m, n);
     }

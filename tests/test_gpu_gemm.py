@@ -140,7 +140,7 @@ def test_ldc_padding_untouched(ctx, cfg):
 @pytest.mark.parametrize("cfg", BF16_CFGS)
 @pytest.mark.parametrize("workers", [1, 3, 7, 0])
 def test_modes_bit_identical_with_traces(ctx, cfg, workers):
-    M, N, K = 1000, 1100, 320
+    M, N, K = 1000, 1104, 320
     A, B = synthetic.gemm_bf16_inputs(M, N, K, seed=15)
     C64, Abs = oracle_full(A, B, M, N, K)
     ref = None
