@@ -41,7 +41,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cfg", type=int, default=0, help="kernel configuration (PGT_CFG_*), 0 = auto")
-    ap.add_argument("--ragged", action="store_true", help="also measure the ragged-tail GEMM set")
+    ap.add_argument("--kernel", default="gemm", choices=["gemm", "add"],
+                    help="headline kernel: the GEMM (default) or the persistent add (for profiling the add)")
     ap.add_argument("--no-extras", action="store_true", help="headline only")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
     return ap.parse_args()
@@ -243,6 +244,8 @@ def run_ours(args, world, rank, local, pg):
     head = desc_for(pgt.SWIZZLED)
     plan = ctx.gemm_plan(head)
     launch = lambda: ctx.gemm_ex(head, dA, dB, dC)  # noqa: E731
+    if args.kernel == "add":
+        return run_add_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peaks)
 
     # ------------------------------------------------------------------ headline
     for _ in range(args.warmup):
@@ -284,6 +287,38 @@ def run_ours(args, world, rank, local, pg):
     if not args.no_extras:
         extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out)
     print(json.dumps(out), flush=True)
+    ctx.close()
+
+
+def run_add_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peaks):
+    """The persistent add (wide tile, blocked) as the timed kernel: GB/s against HBM."""
+    import synthetic
+    x, y = synthetic.add_inputs(ADD_ROWS, ADD_COLS, seed=1)
+    tx, ty = torch.from_numpy(x).to(device), torch.from_numpy(y).to(device)
+    to = torch.empty_like(tx)
+    launch = lambda: ctx.add(tx, ty, to, sched_mode=pgt.BLOCKED)  # noqa: E731
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize()
+    barrier(pg)
+    clocks = Clocks(local)
+    clocks.start()
+    total_ms, per = time_launches(torch, launch, args.steps, 0)
+    clk = clocks.stop()
+    barrier(pg)
+    total_ms = max_over_ranks(pg, total_ms, device)
+    kern_ms = float(np.mean(per))
+    achieved = ADD_BYTES / (kern_ms * 1e-3) / 1e9
+    out = {"metric": "persistent add GB/s vs HBM", "value": world * ADD_BYTES * args.steps / (total_ms * 1e-3) / 1e9,
+           "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "f32", "data": "synthetic",
+           "config": {"workload": "fp32 add 8192x8192, wide 8x1024 tile, blocked", "l2": L2_NOTE},
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": achieved / peaks["hbm_gbs"], "traffic": None},
+           "gpu_launches": args.steps, "clocks": clk}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
     ctx.close()
 
 
