@@ -246,6 +246,30 @@ int pgt_schedule_log(pgt_ctx* ctx, int64_t m_blocks, int64_t n_blocks, int clust
                      int sched_mode, int group_size, int ws_groups, int num_workers,
                      const pgt_trace* trace, void* stream);
 
+/* ------------------------------------------------------ allocation-free GEMM */
+/* No counterpart in the pages: an addition for callers that cannot allocate device memory
+ * (code running inside another runtime's memory-pool or allocator hook, plugins whose
+ * device memory is budgeted up front, real-time paths that forbid allocation after
+ * start-up).  They cannot create a context, because pgt_preamble allocates.
+ *
+ * C = A . B in bf16 with the WORK_STEALING scheduler, exactly as pgt_gemm_ex computes it
+ * (same kernel, so the same bits), on the CURRENT device, with packed leading dimensions
+ * and PGT_CFG_AUTO.  The scratch the kernel needs (ws_groups tile counters, a done counter
+ * and an error word) is a fixed 2304-byte file-scope __device__ array that every GPU which
+ * loads the library holds until the process exits; no call allocates or frees anything.
+ *   A, B, C, M, N, K, b_layout, group_size: as in pgt_gemm (bf16 only).
+ *   ws_groups: 1 .. PGT_NOALLOC_MAX_GROUPS (0 = 8); larger values return PGT_ERR_GROUPS.
+ *   d_err: NULL, or a caller-owned DEVICE int32[4] the kernel writes if a bounded wait
+ *          runs out (code, role, block, site); this call does not clear it.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture.  Every call
+ * clears the counters on `stream` before its launch.  All calls share the one array per
+ * device: calls that overlap on the GPU (different streams, or graph replays running
+ * concurrently) race on it and give wrong results. */
+#define PGT_NOALLOC_MAX_GROUPS 16
+int pgt_gemm_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                     int b_layout, int group_size, int ws_groups, int32_t* d_err, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

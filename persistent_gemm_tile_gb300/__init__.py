@@ -32,8 +32,9 @@ VISIT_FIELDS = 4
 EXPORTS = (
     "pgt_preamble", "pgt_destroy", "pgt_num_sms", "pgt_max_groups", "pgt_last_error", "pgt_strerror",
     "pgt_gemm_workspace_bytes", "pgt_gemm_plan", "pgt_gemm_ex", "pgt_gemm", "pgt_gemm_host",
-    "pgt_add", "pgt_add_workers", "pgt_schedule_log",
+    "pgt_add", "pgt_add_workers", "pgt_schedule_log", "pgt_gemm_noalloc",
 )
+NOALLOC_MAX_GROUPS = 16
 
 
 class GemmDesc(ctypes.Structure):
@@ -91,6 +92,7 @@ def lib() -> ctypes.CDLL:
         L.pgt_add.argtypes = [P, P, P, P, I64, I64, I64, I64, I64, I, I, I, I, P, P]
         L.pgt_add_workers.argtypes = [P, I64, I64, I, I, I]
         L.pgt_schedule_log.argtypes = [P, I64, I64, I, I, I, I, I, P, P]
+        L.pgt_gemm_noalloc.argtypes = [P, P, P, I64, I64, I64, I, I, I, P, P]
         _lib = L
     return _lib
 
@@ -131,6 +133,13 @@ def make_desc(M, N, K, *, lda=0, ldb=0, ldc=0, dtype=BF16, b_layout=B_KN, sched_
         sched_mode = SCHED[sched_mode]
     return GemmDesc(M, N, K, lda, ldb, ldc, dtype, b_layout, sched_mode, group_size, ws_groups, kernel_cfg,
                     num_workers, 0)
+
+
+def gemm_noalloc(A, B, C, M, N, K, b_layout=B_KN, group_size=16, ws_groups=0, err=None, stream=None) -> None:
+    """pgt_gemm_noalloc: the work-stealing bf16 GEMM on the current device for callers that
+    cannot allocate device memory (its scratch is a static array inside the library)."""
+    _check(lib().pgt_gemm_noalloc(_ptr(A), _ptr(B), _ptr(C), M, N, K, b_layout, group_size, ws_groups, _ptr(err),
+                                  _stream(stream)), "pgt_gemm_noalloc")
 
 
 class Context:
