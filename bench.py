@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--kernel", default="gemm", choices=["gemm", "add"],
                     help="headline kernel: the GEMM (default) or the persistent add (for profiling the add)")
     ap.add_argument("--no-extras", action="store_true", help="headline only")
+    ap.add_argument("--ragged", action="store_true",
+                    help="also time the ragged-tail GEMM set per scheduler, with tail idle from traces")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
     return ap.parse_args()
 
@@ -337,6 +339,15 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
         tf = FLOP / (ms * 1e-3) / 1e12
         per_mode[name] = {"tflops": tf, "ms": ms, "frac_of_burst_peak": tf / peaks["bf16_burst"]}
     out["per_mode"] = per_mode
+    # per kernel configuration (swizzled, group 16)
+    per_cfg = {}
+    for cfg, cname in ((pgt.CFG_1CTA_128x128, "1cta_128x128"), (pgt.CFG_1CTA_128x256, "1cta_128x256"),
+                       (pgt.CFG_2CTA_256x128, "2cta_256x128"), (pgt.CFG_2CTA_256x256, "2cta_256x256")):
+        d = desc_for(pgt.SWIZZLED, cfg)
+        _, per = time_launches(torch, lambda: ctx.gemm_ex(d, dA, dB, dC), 40, 5)
+        ms = float(np.median(per))
+        per_cfg[cname] = {"tflops": FLOP / (ms * 1e-3) / 1e12, "ms": ms}
+    out["per_cfg"] = per_cfg
     # tail idle from traced launches (not timed)
     tails = {}
     for mode, name in names.items():
@@ -368,6 +379,31 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
     add["workload"] = "fp32 8192x8192 x,y ~ N(0,1) seed 1, out = x + y"
     out["add"] = add
     del tx, ty, to
+    # MXFP8 block-scaled GEMM 8192^3 (E4M3 payload from N(0,1), E8M0 exponents in [-4, 4], seed 4)
+    qa, sa, qb, sb = synthetic.gemm_mxfp8_inputs(M, N, K, seed=4)
+    tqa, tsa = torch.from_numpy(qa).to(device), torch.from_numpy(sa).to(device)
+    tqb, tsb = torch.from_numpy(qb).to(device), torch.from_numpy(sb).to(device)
+    mx = {}
+    fp8_peak = 2.0 * peaks["bf16_burst"]  # fp8 dense is twice bf16 dense (4.5 vs 2.25 PFLOP/s nominal)
+    for cfg, cname in ((pgt.CFG_2CTA_256x256, "2cta_256x256"), (pgt.CFG_1CTA_128x256, "1cta_128x256"),
+                       (pgt.CFG_2CTA_256x128, "2cta_256x128")):
+        d = pgt.make_desc(M, N, K, dtype=pgt.MXFP8, b_layout=pgt.B_NK, sched_mode=pgt.SWIZZLED, group_size=16,
+                          kernel_cfg=cfg)
+        ws = torch.empty(ctx.gemm_workspace_bytes(d), dtype=torch.uint8, device=device)
+        _, per = time_launches(torch, lambda: ctx.gemm_ex(d, tqa, tqb, dC, sfa=tsa, sfb=tsb, workspace=ws), 40, 5)
+        ms = float(np.median(per))
+        tf = FLOP / (ms * 1e-3) / 1e12
+        mx[cname] = {"tflops": tf, "ms": ms, "frac_of_fp8_peak": tf / fp8_peak}
+    best = max(mx, key=lambda k: mx[k]["tflops"])
+    mx["roofline"] = {"bound": "tensor", "achieved": mx[best]["tflops"], "peak": fp8_peak, "unit": "TFLOP/s",
+                      "frac": mx[best]["tflops"] / fp8_peak, "traffic": None, "kernel": best,
+                      "peak_kind": f"2 x measured bf16 burst ({peaks['source']}), nominal fp8/bf16 ratio"}
+    mx["workload"] = "MXFP8 8192^3, E4M3 payload N(0,1), E8M0 per 1x128 K block, exps U{-4..4}, seed 4, " \
+                     "swizzled group 16; time includes the per-call scale repack"
+    out["mxfp8"] = mx
+    del tqa, tsa, tqb, tsb
+    if args.ragged:
+        out["ragged"] = ragged_set(torch, pgt, ctx, device)
     # end to end from pinned host memory through pgt_gemm_host
     hA = torch.from_numpy(A_host.view(np.int16)).pin_memory()
     hB = torch.from_numpy(B_host.view(np.int16)).pin_memory()
@@ -380,6 +416,37 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
                   "d2h_bytes_per_step": int(hC.numel() * 2), "steps": e2e_steps}
     # the oracle on the host cores
     out["cpu_baseline"] = cpu_baseline(args.cpu_seconds, A_host, B_host)
+
+
+def ragged_set(torch, pgt, ctx, device):
+    """The ragged-tail set (tile counts not a multiple of the SM count), every scheduler:
+    TFLOP/s and tail idle (1 - busy / (workers * span)) from a traced launch."""
+    import synthetic
+    shapes = [(4864, 4096, 2048), (128, 16384, 16384), (3000, 5000, 1024)]
+    res = {}
+    names = {pgt.BLOCKED: "blocked", pgt.INTERLEAVED: "interleaved", pgt.SWIZZLED: "swizzled",
+             pgt.WORK_STEALING: "work_stealing", pgt.BLOCKED_GROUPED_M: "blocked_grouped_m"}
+    for (m, n, k), (a, b) in zip(shapes, synthetic.gemm_bf16_sequence(shapes, seed=3, dist="uniform")):
+        ta = torch.from_numpy(a.view(np.int16)).to(device)
+        tb_ = torch.from_numpy(b.view(np.int16)).to(device)
+        tc = torch.empty((m, n), dtype=torch.int16, device=device)
+        key = f"{m}x{n}x{k}"
+        res[key] = {}
+        for cfg, cname in ((pgt.CFG_1CTA_128x256, "1cta_128x256"), (pgt.CFG_2CTA_256x128, "2cta_256x128")):
+            for mode, name in names.items():
+                d = pgt.make_desc(m, n, k, b_layout=pgt.B_KN, sched_mode=mode, group_size=16, ws_groups=8,
+                                  kernel_cfg=cfg)
+                _, per = time_launches(torch, lambda: ctx.gemm_ex(d, ta, tb_, tc), 20, 3)
+                ms = float(np.median(per))
+                plan = ctx.gemm_plan(d)
+                tr = pgt.TraceBuffers(plan["ctas"], plan["tiles"], device=device)
+                ctx.gemm_ex(d, ta, tb_, tc, trace=tr.struct)
+                torch.cuda.synchronize()
+                res[key][f"{cname}_{name}"] = {"tflops": 2.0 * m * n * k / (ms * 1e-3) / 1e12, "ms": ms,
+                                               "tail_idle": tail_idle(tr.times.cpu().numpy()),
+                                               "tiles": plan["tiles"], "workers": plan["workers"]}
+        del ta, tb_, tc
+    return res
 
 
 def main():

@@ -176,6 +176,8 @@ size_t pgt_gemm_workspace_bytes(const pgt_gemm_desc* desc) {
 
 int pgt_gemm_plan(const pgt_ctx* ctx, const pgt_gemm_desc* desc, pgt_gemm_plan_info* out) {
     pgt_gemm_desc d;
+    if (ctx == nullptr) return PGT_ERR_ARG;
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return PGT_ERR_CUDA;
     return gemm_plan(ctx, desc, &d, out);
 }
 
@@ -184,9 +186,10 @@ int pgt_gemm_ex(pgt_ctx* ctx, const pgt_gemm_desc* desc, const void* A, const vo
                 void* stream) {
     pgt_gemm_desc d;
     pgt_gemm_plan_info plan;
+    if (ctx == nullptr) return PGT_ERR_ARG;
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return PGT_ERR_CUDA;
     int rc = gemm_plan(ctx, desc, &d, &plan);
     if (rc) return rc;
-    if (cudaSetDevice(ctx->device) != cudaSuccess) return PGT_ERR_CUDA;
     return gemm_launch(ctx, d, plan, A, B, sfa, sfb, C, workspace, workspace_bytes, trace,
                        static_cast<cudaStream_t>(stream));
 }
@@ -211,13 +214,14 @@ int pgt_gemm_host(pgt_ctx* ctx, const pgt_gemm_desc* desc, const void* h_A, cons
                   void* workspace, size_t workspace_bytes, void* stream) {
     pgt_gemm_desc d;
     pgt_gemm_plan_info plan;
+    if (ctx == nullptr) return PGT_ERR_ARG;
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return PGT_ERR_CUDA;
     int rc = gemm_plan(ctx, desc, &d, &plan);
     if (rc) return rc;
     if (h_A == nullptr || h_B == nullptr || h_C == nullptr || d_A == nullptr || d_B == nullptr || d_C == nullptr)
         return PGT_ERR_ARG;
     const bool mx = d.dtype == PGT_MXFP8;
     if (mx && (h_sfa == nullptr || h_sfb == nullptr || d_sfa == nullptr || d_sfb == nullptr)) return PGT_ERR_ARG;
-    if (cudaSetDevice(ctx->device) != cudaSuccess) return PGT_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t es = mx ? 1 : 2;
     const size_t b_rows = d.b_layout == PGT_B_KN ? (size_t)d.K : (size_t)d.N;

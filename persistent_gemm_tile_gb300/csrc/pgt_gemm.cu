@@ -1,15 +1,24 @@
 // Persistent tiled GEMM C = A . B for sm_103a: TMA producer warp, tcgen05 MMA warp issuing
-// into double-buffered tensor-memory accumulators, four epilogue warps, an mbarrier
-// stage ring, and a tile-id ring that carries the scheduler's choices to every role.
+// into tensor-memory accumulators, four epilogue warps, an mbarrier stage ring, and a
+// tile-id ring that carries the scheduler's choices to every role.
 //
 // Design source: the warp-specialised persistent kernel of "[Feature] Introduce tile
 // scheduler" (tilelang PR #2441, gemm_mxfp8_blockscaled_1d1d.py): TMA warp, MMA warp,
 // epilogue warpgroup (threads 128..255), loaded/consumed barriers indexed by
 // phase = iter * k_iters + k with stage = phase % stages and parity = (phase / stages) & 1,
-// tmem_full / tmem_empty between MMA and epilogue.  Differences: the accumulator is double
-// buffered in tensor memory so the epilogue of one tile overlaps the next tile's
-// mainloop; the producer runs the scheduler and publishes each tile through a small
-// shared-memory ring (needed for work stealing, where roles cannot recompute the tile).
+// tmem_full / tmem_empty between MMA and epilogue, 2-CTA clusters where CTA cta_id of a
+// pair owns tile row bx = m_idx * 2 + cta_id and loads half of B's tile, and MXFP8 scales
+// (one E8M0 byte per row and 128-wide K block) copied to tensor memory for block-scaled
+// MMAs.  Differences: the accumulator is double buffered whenever tensor memory allows, so
+// the epilogue of one tile overlaps the next tile's mainloop; the producer runs the
+// scheduler and publishes each tile through a small shared-memory ring (needed for work
+// stealing, where roles cannot recompute the tile); scales are repacked once per call into
+// the tensor-memory copy layout, so no transpose warp is needed.
+//
+// Template parameters: CS = CTAs per worker (1, or 2 for a cluster pair issuing
+// cta_group::2 MMAs with M = 256); BN = output columns per worker tile; B_MN = B stored
+// K x N (N contiguous) instead of N x K; MX = MXFP8 operands (E4M3 + E8M0 scales) instead
+// of bf16; TRACE = record every visit.
 #include <cuda_bf16.h>
 #include <stdio.h>
 
@@ -24,38 +33,64 @@ struct GemmParams {
     int k_iters;
     SchedParams sp;
     int* err;
+    int sfa_rows;  // MXFP8: rows of 128-row scale blocks per k group in the packed SFA
+    int sfb_rows;  // MXFP8: same for SFB
     int32_t* tr_visits;
     int64_t tr_max;
     int32_t* tr_counts;
     int64_t* tr_times;
 };
 
-constexpr int kThreads = 256;     // warp 0 producer, warp 1 MMA, warps 4-7 epilogue
-constexpr int kTileRing = 4;      // tile-id ring depth
+constexpr int kThreads = 256;           // warp 0 producer, warp 1 MMA, warps 4-7 epilogue
+constexpr int kTileRing = 4;            // tile-id ring depth
 constexpr int kEpiWarps = 4;
 constexpr int kEpiBufBytes = 32 * 128;  // 32 rows x 64 bf16, 128B-swizzled, per buffer
+constexpr int kMaxSmem = 232448;        // 227 KB dynamic shared memory per CTA
 
-// Shared-memory layout of the 1-CTA bf16 kernel (offsets from a 1024-aligned base).
-template <int BN, int STAGES>
-struct Bf16Layout {
-    static constexpr int BM = 128, BK = 64;
-    static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int pow2_at_least(int v) {
+    int p = 32;
+    while (p < v) p *= 2;
+    return p;
+}
+
+// Shared-memory and tensor-memory layout (offsets from a 1024-aligned base).  Every stage
+// holds this CTA's 128 x 128-byte A slice, its BN/CS rows (or columns) of B, and for MXFP8
+// a scale area refilled every fourth stage.
+template <int CS, int BN, int STAGES, bool MX>
+struct Layout {
+    static constexpr int BM = 128;                 // rows per CTA
+    static constexpr int BK = MX ? 128 : 64;       // K elements per stage (128 bytes per row)
+    static constexpr int BN_CTA = BN / CS;         // B rows (or columns) held by one CTA
+    static constexpr int A_BYTES = BM * 128;
+    static constexpr int B_BYTES = BN_CTA * 128;
+    static constexpr int NB128 = (BN + 127) / 128;  // 128-row scale blocks of B per tile
+    static constexpr int SF_BYTES = MX ? ((512 + 512 * NB128 + 1023) / 1024 * 1024) : 0;
+    static constexpr int SFB_OFF = A_BYTES + B_BYTES + 512;  // SFA at A+B, SFB after it
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
+    static constexpr int TX_BYTES = A_BYTES + B_BYTES;             // per CTA, every stage
+    static constexpr int SF_TX_BYTES = MX ? 512 + 512 * NB128 : 0;  // per CTA, every 4th stage
+    // accumulators: double buffered unless tensor memory cannot hold two plus the scales
+    static constexpr int SF_COLS = MX ? 2 * (4 + 4 * NB128) : 0;
+    static constexpr int ACC_BUFS = (2 * BN + SF_COLS <= 512) ? 2 : 1;
+    static constexpr int SFA_COL = ACC_BUFS * BN;
+    static constexpr int SFB_COL = SFA_COL + 8;
+    static constexpr int TMEM_COLS = pow2_at_least(ACC_BUFS * BN + SF_COLS);
+    static constexpr int EPI_BUFS = (STAGES * STAGE_BYTES + kEpiWarps * 2 * kEpiBufBytes + 2048 <= kMaxSmem) ? 2 : 1;
     static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
-    static constexpr int BAR_OFF = EPI_OFF + kEpiWarps * 2 * kEpiBufBytes;
+    static constexpr int BAR_OFF = EPI_OFF + kEpiWarps * EPI_BUFS * kEpiBufBytes;
     // barriers: full[S], empty[S], tfull[2], tempty[2], sfull[Q], sempty[Q], mma_done
     static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * kTileRing + 1;
-    // the ring holds int4 entries: 16-byte aligned
-    static constexpr int RING_OFF = BAR_OFF + (NUM_BARS * 8 + 15) / 16 * 16;
-    static constexpr int MISC_OFF = RING_OFF + kTileRing * 16;  // tmem slot, abort flag
+    static constexpr int RING_OFF = BAR_OFF + (NUM_BARS * 8 + 15) / 16 * 16;  // int4 entries
+    static constexpr int MISC_OFF = RING_OFF + kTileRing * 16;                // tmem slot, abort flag
     static constexpr int BYTES = MISC_OFF + 16;
     static constexpr int SMEM = BYTES + 1024;  // alignment slack
-    static constexpr int TMEM_COLS = 2 * BN;
-    static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
+    static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0 && (A_BYTES + B_BYTES) % 1024 == 0,
+                  "stages must keep 1024-byte swizzle alignment");
     static_assert(EPI_OFF % 1024 == 0 && BAR_OFF % 1024 == 0, "epilogue buffers need 1024-byte alignment");
     static_assert(RING_OFF % 16 == 0 && MISC_OFF % 16 == 0, "ring entries are 16-byte vectors");
-    static_assert(SMEM <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
+    static_assert(SMEM <= kMaxSmem, "dynamic shared memory above the 227 KB per-CTA limit");
+    static_assert(TMEM_COLS <= 512, "tensor memory holds 512 columns");
+    static_assert(BN_CTA % 64 == 0, "B is loaded in 64-wide boxes");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
@@ -68,13 +103,31 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
-// bf16 GEMM, one CTA per worker, 128 x BN output tiles, K step 64 per stage.
-// B_MN: B stored K x N (N contiguous); otherwise N x K (K contiguous).
-template <int BN, int STAGES, bool B_MN, bool TRACE>
+// TMA load whose completion goes to `bar`: plain form for one CTA, pair form (the barrier
+// may be the leader's) for a cluster pair.
+template <int CS>
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x, int32_t y) {
+    if constexpr (CS == 1)
+        tma_load_2d(dst, map, bar, x, y);
+    else
+        tma_load_2d_pair(dst, map, bar, x, y);
+}
+
+// Arrive on a barrier of this CTA, or on the same barrier of the pair's leader.
+__device__ __forceinline__ void arrive_local_or_leader(uint32_t local_bar, bool remote) {
+    if (remote)
+        mbar_arrive_remote(mapa_shared(local_bar, 0));
+    else
+        mbar_arrive(local_bar);
+}
+
+template <int CS, int BN, int STAGES, bool B_MN, bool MX, bool TRACE>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_bf16_1cta_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                          const __grid_constant__ CUtensorMap tmC, const GemmParams gp) {
-    using L = Bf16Layout<BN, STAGES>;
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmSFA,
+                const __grid_constant__ CUtensorMap tmSFB, const GemmParams gp) {
+    using L = Layout<CS, BN, STAGES, MX>;
+    constexpr bool kPair = CS == 2;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -82,6 +135,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const uint32_t lane = lane_id();
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // CTA index inside the pair
+    const bool leader = rank == 0;
+    const int worker = blockIdx.x / CS;
 
     const uint32_t bar0 = base + L::BAR_OFF;
     auto full = [&](int s) { return bar0 + 8u * s; };
@@ -97,27 +153,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full(s), 1);
-            mbar_init(empty(s), 1);
+            mbar_init(full(s), 1);   // the leader's expect_tx; bytes of both CTAs of a pair
+            mbar_init(empty(s), 1);  // one MMA commit
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull(a), 1);
-            mbar_init(tempty(a), kEpiWarps);
+            mbar_init(tempty(a), kEpiWarps * CS);
         }
         for (int q = 0; q < kTileRing; ++q) {
             mbar_init(sfull(q), 1);
-            mbar_init(sempty(q), 1 + kEpiWarps);
+            // consumers of a ring entry: the MMA thread, the epilogue warps, and in a pair
+            // also the peer's producer and epilogue warps (all counted on the leader)
+            mbar_init(sempty(q), kPair ? 2 + 2 * kEpiWarps : 1 + kEpiWarps);
         }
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc<1>(base + L::MISC_OFF, L::TMEM_COLS);
-        tmem_relinquish<1>();
+        tmem_alloc<CS>(base + L::MISC_OFF, L::TMEM_COLS);
+        tmem_relinquish<CS>();
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (kPair)
+        cluster_sync();
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -128,19 +189,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             prefetch_tensormap(&tmA);
             prefetch_tensormap(&tmB);
+            if constexpr (MX) {
+                prefetch_tensormap(&tmSFA);
+                prefetch_tensormap(&tmSFB);
+            }
             Scheduler sch;
-            sch.init(gp.sp, blockIdx.x);
+            if (leader) sch.init(gp.sp, worker);
             uint32_t it = 0, qc = 0;
             int nvis = 0;
             bool ok = true;
             while (ok) {
-                int t = *abort_flag ? -1 : sch.fetch();
-                int m = 0, n = 0;
-                if (t >= 0) decode_tile(gp.sp, t, m, n);
+                int t, m = 0, n = 0;
                 const int q = qc % kTileRing;
-                if (!mbar_wait(sempty(q), ((qc / kTileRing) & 1u) ^ 1u, abort_flag, gp.err, kRoleProducer, 0)) break;
-                ring[q] = make_int4(t, m, n, 0);
-                mbar_arrive(sfull(q));
+                const uint32_t qpar = (qc / kTileRing) & 1u;
+                if (leader) {
+                    t = *abort_flag ? -1 : sch.fetch();
+                    if (t >= 0) decode_tile(gp.sp, t, m, n);
+                    if (!mbar_wait<kPair>(sempty(q), qpar ^ 1u, abort_flag, gp.err, kRoleProducer, 0)) break;
+                    ring[q] = make_int4(t, m, n, 0);
+                    if constexpr (kPair) {
+                        const uint32_t ring_addr = smem_u32(ring + q);
+                        st_shared_cluster_v4(mapa_shared(ring_addr, 1), t, m, n, 0);
+                        mbar_arrive_remote(mapa_shared(sfull(q), 1));
+                    }
+                    mbar_arrive(sfull(q));
+                } else {
+                    if (!mbar_wait<true>(sfull(q), qpar, abort_flag, gp.err, kRoleProducer, 8)) break;
+                    const int4 e = ring[q];
+                    t = e.x;
+                    m = e.y;
+                    n = e.z;
+                    mbar_arrive_remote(mapa_shared(sempty(q), 0));
+                }
                 ++qc;
                 if (t < 0) break;
                 if (TRACE && gp.tr_visits != nullptr) {
@@ -153,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ++nvis;
                 }
-                const int m0 = m * L::BM;
-                const int n0 = n * BN;
+                const int row0 = (m * CS + (int)rank) * L::BM;  // this CTA's rows of A
+                const int col0 = n * BN + (int)rank * L::BN_CTA;  // this CTA's slice of B
                 for (int k = 0; k < gp.k_iters; ++k, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
@@ -164,24 +244,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t sa = base + s * L::STAGE_BYTES;
                     const uint32_t sb = sa + L::A_BYTES;
-                    mbar_arrive_expect_tx(full(s), L::STAGE_BYTES);
-                    tma_load_2d(sa, &tmA, full(s), k * L::BK, m0);
+                    const bool sf_now = MX && (k & 3) == 0;
+                    if (leader) mbar_arrive_expect_tx(full(s), CS * (L::TX_BYTES + (sf_now ? L::SF_TX_BYTES : 0)));
+                    const uint32_t fb = kPair ? mapa_shared(full(s), 0) : full(s);
+                    tma_load<CS>(sa, &tmA, fb, k * L::BK, row0);
                     if constexpr (B_MN) {
 #pragma unroll
-                        for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * 8192, &tmB, full(s), n0 + 64 * j, k * L::BK);
+                        for (int j = 0; j < L::BN_CTA / 64; ++j)
+                            tma_load<CS>(sb + j * 8192, &tmB, fb, col0 + 64 * j, k * L::BK);
                     } else {
-                        tma_load_2d(sb, &tmB, full(s), k * L::BK, n0);
+                        tma_load<CS>(sb, &tmB, fb, k * L::BK, col0);
+                    }
+                    if constexpr (MX) {
+                        if (sf_now) {
+                            const int kg = k >> 2;
+                            tma_load<CS>(sb + L::B_BYTES, &tmSFA, fb, 0, kg * gp.sfa_rows + m * CS + (int)rank);
+                            tma_load<CS>(sa + L::SFB_OFF, &tmSFB, fb, 0, kg * gp.sfb_rows + n * L::NB128);
+                        }
                     }
                 }
             }
-            sch.finish();
+            if (leader) sch.finish();
             if (TRACE && gp.tr_counts != nullptr) gp.tr_counts[blockIdx.x] = nvis;
         }
         __syncwarp();
     } else if (warp == 1) {
         // ----------------------------------------------------------------- MMA
-        if (lane == 0) {
-            constexpr uint32_t idesc = make_idesc_bf16(128, BN, false, B_MN);
+        if (leader && lane == 0) {
             uint32_t it = 0, qc = 0, tc = 0;
             bool ok = true;
             while (ok) {
@@ -191,14 +280,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(sempty(q));
                 ++qc;
                 if (t < 0) break;
-                const int acc = tc & 1;
-                if (!mbar_wait(tempty(acc), ((tc >> 1) & 1u) ^ 1u, abort_flag, gp.err, kRoleMma, 3)) break;
+                const int acc = tc % L::ACC_BUFS;
+                if (!mbar_wait<kPair>(tempty(acc), ((tc / L::ACC_BUFS) & 1u) ^ 1u, abort_flag, gp.err, kRoleMma, 3))
+                    break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * BN;
                 for (int k = 0; k < gp.k_iters; ++k, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
-                    if (!mbar_wait(full(s), ph, abort_flag, gp.err, kRoleMma, 4)) {
+                    if (!mbar_wait<kPair>(full(s), ph, abort_flag, gp.err, kRoleMma, 4)) {
                         ok = false;
                         break;
                     }
@@ -208,22 +298,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t adesc = make_smem_desc(sa, 16, 1024, kLayoutSw128);
                     const uint64_t bdesc = B_MN ? make_smem_desc(sb, 8192, 1024, kLayoutSw128)
                                                 : make_smem_desc(sb, 16, 1024, kLayoutSw128);
+                    if constexpr (MX) {
+                        const uint32_t buf = (k >> 2) & 1;
+                        const uint32_t sfa_t = tmem_base + L::SFA_COL + 4 * buf;
+                        const uint32_t sfb_t = tmem_base + L::SFB_COL + 4 * L::NB128 * buf;
+                        if ((k & 3) == 0) {
+                            // scales of the next four K blocks: smem -> tensor memory
+                            tmem_cp_32x128b_x4<CS>(sfa_t, make_smem_desc(sb + L::B_BYTES, 0, 128, kLayoutNone));
 #pragma unroll
-                    for (int kk = 0; kk < L::BK / 16; ++kk) {
-                        // K-major operands advance 16 elements = 32 bytes inside the
-                        // 128-byte swizzle row; the MN-major B advances 16 rows of 128 bytes.
-                        const uint64_t a_k = adesc + (uint64_t)(2 * kk);
-                        const uint64_t b_k = bdesc + (uint64_t)(B_MN ? 128 * kk : 2 * kk);
-                        mma_bf16<1>(d, a_k, b_k, idesc, (k | kk) != 0 ? 1u : 0u);
+                            for (int b = 0; b < L::NB128; ++b)
+                                tmem_cp_32x128b_x4<CS>(sfb_t + 4 * b,
+                                                       make_smem_desc(sa + L::SFB_OFF + 512 * b, 0, 128, kLayoutNone));
+                        }
+                        // every 32-wide MMA of this 128-wide K block uses the block's scale byte
+                        const uint32_t idesc = make_idesc_mxf8(128 * CS, BN, k & 3, k & 3);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_mxf8<CS>(d, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc, sfa_t, sfb_t,
+                                         (k | kk) != 0 ? 1u : 0u);
+                    } else {
+                        constexpr uint32_t idesc = make_idesc_bf16(128 * CS, BN, false, B_MN);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            // K-major operands advance 16 elements = 32 bytes inside the
+                            // 128-byte swizzle row; the MN-major B advances 16 rows of 128 bytes.
+                            const uint64_t a_k = adesc + (uint64_t)(2 * kk);
+                            const uint64_t b_k = bdesc + (uint64_t)(B_MN ? 128 * kk : 2 * kk);
+                            mma_bf16<CS>(d, a_k, b_k, idesc, (k | kk) != 0 ? 1u : 0u);
+                        }
                     }
-                    mma_commit(empty(s));
+                    if constexpr (kPair)
+                        mma_commit_pair(empty(s), 3);
+                    else
+                        mma_commit(empty(s));
                 }
                 if (!ok) break;
-                mma_commit(tfull(acc));
+                if constexpr (kPair)
+                    mma_commit_pair(tfull(acc), 3);
+                else
+                    mma_commit(tfull(acc));
                 ++tc;
             }
             // every MMA issued above has completed once this barrier flips
-            mma_commit(mma_done);
+            if constexpr (kPair)
+                mma_commit_pair(mma_done, 1);
+            else
+                mma_commit(mma_done);
             volatile int no_abort = 0;
             mbar_wait(mma_done, 0, &no_abort, gp.err, kRoleMma, 5);
         }
@@ -231,20 +351,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 4) {
         // ------------------------------------------------------------ epilogue
         const int qw = warp - 4;  // TMEM lane quarter this warp may access
-        const uint32_t epi = base + L::EPI_OFF + qw * 2 * kEpiBufBytes;
+        const uint32_t epi = base + L::EPI_OFF + qw * L::EPI_BUFS * kEpiBufBytes;
         uint32_t qc = 0, tc = 0, chunk = 0;
         while (true) {
             const int q = qc % kTileRing;
-            if (!mbar_wait(sfull(q), (qc / kTileRing) & 1u, abort_flag, gp.err, kRoleEpilogue, 6)) break;
+            if (!mbar_wait<kPair>(sfull(q), (qc / kTileRing) & 1u, abort_flag, gp.err, kRoleEpilogue, 6)) break;
             const int4 e = ring[q];
             __syncwarp();
-            if (lane == 0) mbar_arrive(sempty(q));
+            if (lane == 0) arrive_local_or_leader(sempty(q), !leader);
             ++qc;
             if (e.x < 0) break;
-            const int acc = tc & 1;
-            if (!mbar_wait(tfull(acc), (tc >> 1) & 1u, abort_flag, gp.err, kRoleEpilogue, 7)) break;
+            const int acc = tc % L::ACC_BUFS;
+            if (!mbar_wait<kPair>(tfull(acc), (tc / L::ACC_BUFS) & 1u, abort_flag, gp.err, kRoleEpilogue, 7)) break;
             tc_fence_after();
-            const int row0 = e.y * L::BM + 32 * qw;
+            const int row0 = (e.y * CS + (int)rank) * L::BM + 32 * qw;
             const int col0 = e.z * BN;
             const uint32_t tacc = tmem_base + ((uint32_t)(32 * qw) << 16) + acc * BN;
 #pragma unroll 1
@@ -257,10 +377,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // accumulator fully read: hand it back to the MMA warp
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(tempty(acc));
+                    if (lane == 0) arrive_local_or_leader(tempty(acc), !leader);
                 }
-                const uint32_t buf = epi + (chunk & 1u) * kEpiBufBytes;
-                if (lane == 0) bulk_wait_read<1>();
+                const uint32_t buf = epi + (chunk % L::EPI_BUFS) * kEpiBufBytes;
+                if (lane == 0) {
+                    if constexpr (L::EPI_BUFS == 2)
+                        bulk_wait_read<1>();
+                    else
+                        bulk_wait_read<0>();
+                }
                 __syncwarp();
                 const uint32_t rowaddr = buf + lane * 128u;
 #pragma unroll
@@ -289,11 +414,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     }
 
-    __syncthreads();
+    if constexpr (kPair)
+        cluster_sync();
+    else
+        __syncthreads();
     if (TRACE && threadIdx.x == 0 && gp.tr_times != nullptr) gp.tr_times[2 * blockIdx.x + 1] = (int64_t)globaltimer();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc<1>(tmem_base, L::TMEM_COLS);
+        tmem_dealloc<CS>(tmem_base, L::TMEM_COLS);
+    }
+}
+
+// MXFP8 scales: plain [rows][K/128] bytes -> for each group of four 128-wide K blocks and
+// each block of 128 rows, 512 bytes in the tensor-memory copy layout (byte
+// lane*16 + c*4 + j holds row c*32 + lane, K block 4*group + j; zero past the edges).
+// Output row (group * blocks + block) is one 128-word line: group-major, row-block minor.
+__global__ void sf_repack_kernel(const uint8_t* __restrict__ sfa, const uint8_t* __restrict__ sfb, int M, int N,
+                                 int kb, int kgroups, int ma, int nb, uint32_t* __restrict__ outa,
+                                 uint32_t* __restrict__ outb) {
+    const int64_t words_a = (int64_t)kgroups * ma * 128;
+    const int64_t words_b = (int64_t)kgroups * nb * 128;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < words_a + words_b;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const bool is_a = idx < words_a;
+        const int64_t i = is_a ? idx : idx - words_a;
+        const int blocks = is_a ? ma : nb;
+        const int rows = is_a ? M : N;
+        const uint8_t* src = is_a ? sfa : sfb;
+        const int w = (int)(i & 127);
+        const int64_t line = i >> 7;
+        const int blk = (int)(line % blocks);
+        const int kg = (int)(line / blocks);
+        const int r = blk * 128 + (w & 3) * 32 + (w >> 2);
+        uint32_t v = 0;
+        if (r < rows) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int kbi = kg * 4 + j;
+                if (kbi < kb) v |= (uint32_t)src[(int64_t)r * kb + kbi] << (8 * j);
+            }
+        }
+        (is_a ? outa : outb)[i] = v;
     }
 }
 
@@ -318,55 +479,134 @@ EncodeTiledFn encode_fn() {
 }
 
 inline int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Stage counts per configuration (the Layout static_asserts check they fit).
+template <int CS, int BN, bool MX>
+struct Stages;
+template <> struct Stages<1, 128, false> { static constexpr int value = 6; };
+template <> struct Stages<1, 256, false> { static constexpr int value = 4; };
+template <> struct Stages<2, 128, false> { static constexpr int value = 8; };
+template <> struct Stages<2, 256, false> { static constexpr int value = 6; };
+template <> struct Stages<1, 128, true> { static constexpr int value = 5; };
+template <> struct Stages<1, 256, true> { static constexpr int value = 4; };
+template <> struct Stages<2, 128, true> { static constexpr int value = 7; };
+template <> struct Stages<2, 256, true> { static constexpr int value = 6; };
 
 struct CfgShape {
-    int bm, bn, bk, cs, stages, smem;
+    int cs, bn, stages, smem, bk;
 };
 
+template <int CS, int BN, bool MX>
+CfgShape shape_of() {
+    using L = Layout<CS, BN, Stages<CS, BN, MX>::value, MX>;
+    return {CS, BN, Stages<CS, BN, MX>::value, L::SMEM, L::BK};
+}
+
 bool cfg_shape(int cfg, int dtype, CfgShape* s) {
-    if (dtype == PGT_BF16) {
-        switch (cfg) {
-            case PGT_CFG_1CTA_128x128:
-                *s = {128, 128, 64, 1, 6, Bf16Layout<128, 6>::SMEM};
-                return true;
-            case PGT_CFG_1CTA_128x256:
-                *s = {128, 256, 64, 1, 4, Bf16Layout<256, 4>::SMEM};
-                return true;
-            default:
-                return false;
-        }
+    const bool mx = dtype == PGT_MXFP8;
+    switch (cfg) {
+        case PGT_CFG_1CTA_128x128: *s = mx ? shape_of<1, 128, true>() : shape_of<1, 128, false>(); return true;
+        case PGT_CFG_1CTA_128x256: *s = mx ? shape_of<1, 256, true>() : shape_of<1, 256, false>(); return true;
+        case PGT_CFG_2CTA_256x128: *s = mx ? shape_of<2, 128, true>() : shape_of<2, 128, false>(); return true;
+        case PGT_CFG_2CTA_256x256: *s = mx ? shape_of<2, 256, true>() : shape_of<2, 256, false>(); return true;
+        default: return false;
     }
-    return false;
 }
 
-template <int BN, int S, bool BMN, bool TR>
-int launch_bf16_1cta(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmParams& gp,
-                     int ctas, int device, cudaStream_t st) {
-    auto kern = gemm_bf16_1cta_kernel<BN, S, BMN, TR>;
-    constexpr int smem = Bf16Layout<BN, S>::SMEM;
-    static bool attr_done[64] = {};
-    if (device < 0 || device >= 64) return PGT_ERR_ARG;
-    if (!attr_done[device]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, GemmParams);
+
+template <int CS, int BN, bool BMN, bool MX, bool TR>
+KernelFn kernel_ptr() {
+    return reinterpret_cast<KernelFn>(&gemm_kernel<CS, BN, Stages<CS, BN, MX>::value, BMN, MX, TR>);
+}
+
+template <int CS, int BN, bool MX>
+KernelFn pick_layout_trace(bool bmn, bool tr) {
+    if constexpr (MX) {
+        return tr ? kernel_ptr<CS, BN, false, true, true>() : kernel_ptr<CS, BN, false, true, false>();
+    } else {
+        if (bmn) return tr ? kernel_ptr<CS, BN, true, false, true>() : kernel_ptr<CS, BN, true, false, false>();
+        return tr ? kernel_ptr<CS, BN, false, false, true>() : kernel_ptr<CS, BN, false, false, false>();
+    }
+}
+
+KernelFn pick_kernel(int cfg, bool mx, bool bmn, bool tr) {
+    switch (cfg) {
+        case PGT_CFG_1CTA_128x128: return mx ? pick_layout_trace<1, 128, true>(bmn, tr) : pick_layout_trace<1, 128, false>(bmn, tr);
+        case PGT_CFG_1CTA_128x256: return mx ? pick_layout_trace<1, 256, true>(bmn, tr) : pick_layout_trace<1, 256, false>(bmn, tr);
+        case PGT_CFG_2CTA_256x128: return mx ? pick_layout_trace<2, 128, true>(bmn, tr) : pick_layout_trace<2, 128, false>(bmn, tr);
+        case PGT_CFG_2CTA_256x256: return mx ? pick_layout_trace<2, 256, true>(bmn, tr) : pick_layout_trace<2, 256, false>(bmn, tr);
+        default: return nullptr;
+    }
+}
+
+constexpr int kMaxDevices = 64;
+constexpr int kNumCfgSlots = 5 * 2 * 2 * 2;  // cfg x mx x bmn x trace
+
+// Per device and kernel: dynamic shared memory attribute set, and how many workers
+// (CTAs or CTA pairs) fit on the GPU at once.
+struct KernelInfo {
+    bool ready;
+    int max_workers;
+};
+KernelInfo g_kinfo[kMaxDevices][kNumCfgSlots];
+
+int kernel_info(int device, int cfg, bool mx, bool bmn, bool tr, const CfgShape& s, KernelInfo* out) {
+    if (device < 0 || device >= kMaxDevices) return PGT_ERR_ARG;
+    const int slot = ((cfg * 2 + (int)mx) * 2 + (int)bmn) * 2 + (int)tr;
+    KernelInfo& ki = g_kinfo[device][slot];
+    if (!ki.ready) {
+        KernelFn k = pick_kernel(cfg, mx, bmn, tr);
+        if (k == nullptr) return PGT_ERR_UNSUPPORTED;
+        if (cudaFuncSetAttribute(reinterpret_cast<const void*>(k), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 s.smem) != cudaSuccess)
             return PGT_ERR_CUDA;
-        attr_done[device] = true;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return PGT_ERR_CUDA;
+        int workers = sms / s.cs;
+        if (s.cs > 1) {
+            cudaLaunchConfig_t lc = {};
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = s.cs;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            lc.gridDim = dim3(s.cs * workers, 1, 1);
+            lc.blockDim = dim3(kThreads, 1, 1);
+            lc.dynamicSmemBytes = s.smem;
+            lc.attrs = at;
+            lc.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void*>(k), &lc) == cudaSuccess &&
+                clusters > 0)
+                workers = clusters;
+            cudaGetLastError();
+        }
+        ki.max_workers = workers > 0 ? workers : 1;
+        ki.ready = true;
     }
-    kern<<<ctas, kThreads, smem, st>>>(ta, tb, tc, gp);
-    return cuda_status(cudaGetLastError());
+    *out = ki;
+    return PGT_OK;
 }
 
-template <int BN, int S>
-int dispatch_bf16_1cta(bool bmn, bool trace, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
-                       const GemmParams& gp, int ctas, int device, cudaStream_t st) {
-    if (bmn) {
-        return trace ? launch_bf16_1cta<BN, S, true, true>(ta, tb, tc, gp, ctas, device, st)
-                     : launch_bf16_1cta<BN, S, true, false>(ta, tb, tc, gp, ctas, device, st);
-    }
-    return trace ? launch_bf16_1cta<BN, S, false, true>(ta, tb, tc, gp, ctas, device, st)
-                 : launch_bf16_1cta<BN, S, false, false>(ta, tb, tc, gp, ctas, device, st);
-}
+// Packed-scale workspace geometry: k groups of four 128-wide K blocks, 128-row blocks of
+// A and B rounded up to even counts (pairs of CTAs).
+struct SfGeometry {
+    int kb, kgroups, ma, nb;
+    size_t bytes_a, bytes_b;
+};
 
-inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+SfGeometry sf_geometry(int64_t M, int64_t N, int64_t K) {
+    SfGeometry g;
+    g.kb = (int)(K / 128);
+    g.kgroups = (g.kb + 3) / 4;
+    g.ma = (int)((cdiv64(M, 128) + 1) / 2 * 2);
+    g.nb = (int)((cdiv64(N, 128) + 1) / 2 * 2);
+    g.bytes_a = (size_t)g.kgroups * g.ma * 512;
+    g.bytes_b = (size_t)g.kgroups * g.nb * 512;
+    return g;
+}
 
 }  // namespace
 
@@ -384,8 +624,9 @@ int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, u
 }
 
 size_t gemm_workspace_bytes(const pgt_gemm_desc& d) {
-    (void)d;
-    return 0;
+    if (d.dtype != PGT_MXFP8 || d.M < 1 || d.N < 1 || d.K < 128 || d.K % 128) return 0;
+    const SfGeometry g = sf_geometry(d.M, d.N, d.K);
+    return g.bytes_a + g.bytes_b;
 }
 
 int gemm_plan(const pgt_ctx* ctx, const pgt_gemm_desc* in, pgt_gemm_desc* d, pgt_gemm_plan_info* p) {
@@ -411,23 +652,28 @@ int gemm_plan(const pgt_ctx* ctx, const pgt_gemm_desc* in, pgt_gemm_desc* d, pgt
     if (d->dtype == PGT_MXFP8) {
         if (d->K % 128 != 0 || d->b_layout != PGT_B_NK) return PGT_ERR_ARG;
     }
-    if (d->kernel_cfg == PGT_CFG_AUTO) d->kernel_cfg = d->dtype == PGT_BF16 ? PGT_CFG_1CTA_128x256 : PGT_CFG_AUTO;
+    if (d->kernel_cfg == PGT_CFG_AUTO)
+        d->kernel_cfg = PGT_CFG_2CTA_256x256;  // fastest measured for bf16 and MXFP8 alike
     CfgShape s;
     if (!cfg_shape(d->kernel_cfg, d->dtype, &s)) return PGT_ERR_UNSUPPORTED;
-    const int64_t m_blocks = cdiv64(d->M, s.bm);
+    const int64_t m_blocks = cdiv64(d->M, 128);
     const int64_t n_blocks = cdiv64(d->N, s.bn);
     const int64_t m_tiles = cdiv64(m_blocks, s.cs);
     const int64_t tiles = m_tiles * n_blocks;
     if (tiles >= lim) return PGT_ERR_ARG;
     int64_t workers = d->num_workers;
     if (workers == 0) {
-        workers = ctx->num_sms / s.cs;
+        KernelInfo ki;
+        int rc = kernel_info(ctx->device, d->kernel_cfg, d->dtype == PGT_MXFP8, d->b_layout == PGT_B_KN, false, s,
+                             &ki);
+        if (rc) return rc;
+        workers = ki.max_workers;
         if (workers > tiles) workers = tiles;
         if (workers < 1) workers = 1;
     }
     if (workers * s.cs >= lim) return PGT_ERR_ARG;
     p->kernel_cfg = d->kernel_cfg;
-    p->bm = s.bm;
+    p->bm = 128;
     p->bn = s.bn;
     p->bk = s.bk;
     p->cluster_size = s.cs;
@@ -446,15 +692,24 @@ int gemm_plan(const pgt_ctx* ctx, const pgt_gemm_desc* in, pgt_gemm_desc* d, pgt
 int gemm_launch(pgt_ctx* ctx, const pgt_gemm_desc& d, const pgt_gemm_plan_info& plan, const void* A, const void* B,
                 const uint8_t* sfa, const uint8_t* sfb, void* C, void* workspace, size_t workspace_bytes,
                 const pgt_trace* trace, cudaStream_t stream) {
+    const bool mx = d.dtype == PGT_MXFP8;
     if (A == nullptr || B == nullptr || C == nullptr) return PGT_ERR_ARG;
     if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return PGT_ERR_ALIGN;
-    if (d.dtype == PGT_BF16 && (sfa != nullptr || sfb != nullptr)) return PGT_ERR_ARG;
+    if (!mx && (sfa != nullptr || sfb != nullptr)) return PGT_ERR_ARG;
+    if (mx && (sfa == nullptr || sfb == nullptr)) return PGT_ERR_ARG;
     const size_t ws_need = gemm_workspace_bytes(d);
-    if (ws_need > 0 && (workspace == nullptr || workspace_bytes < ws_need)) return PGT_ERR_WORKSPACE;
+    if (ws_need > 0 && (workspace == nullptr || workspace_bytes < ws_need || !aligned16(workspace)))
+        return PGT_ERR_WORKSPACE;
     if (trace != nullptr) {
         if (trace->visits == nullptr || trace->counts == nullptr || trace->max_visits < 1) return PGT_ERR_ARG;
     }
-    if (d.dtype != PGT_BF16 || plan.cluster_size != 1) return PGT_ERR_UNSUPPORTED;
+    CfgShape s;
+    if (!cfg_shape(plan.kernel_cfg, d.dtype, &s)) return PGT_ERR_UNSUPPORTED;
+    const bool bmn = d.b_layout == PGT_B_KN;
+    const bool tr = trace != nullptr;
+    KernelInfo ki;
+    int rc = kernel_info(ctx->device, plan.kernel_cfg, mx, bmn, tr, s, &ki);
+    if (rc) return rc;
 
     GemmParams gp;
     gp.M = (int)d.M;
@@ -477,38 +732,77 @@ int gemm_launch(pgt_ctx* ctx, const pgt_gemm_desc& d, const pgt_gemm_plan_info& 
     gp.sp.counters = ctx->d_counters;
     gp.sp.done = ctx->d_done;
     gp.err = ctx->d_err;
+    gp.sfa_rows = 0;
+    gp.sfb_rows = 0;
     gp.tr_visits = trace ? trace->visits : nullptr;
     gp.tr_max = trace ? trace->max_visits : 0;
     gp.tr_counts = trace ? trace->counts : nullptr;
     gp.tr_times = trace ? trace->times_ns : nullptr;
 
     if (d.sched_mode == PGT_WORK_STEALING && (ctx->flags & PGT_FLAG_HOST_RESET)) {
-        if (cudaMemsetAsync(ctx->d_counters, 0, sizeof(int) * 32 * (ctx->max_groups + 1), stream) != cudaSuccess)
+        if (cudaMemsetAsync(ctx->d_counters, 0, sizeof(int) * kCounterStride * (ctx->max_groups + 1), stream) !=
+            cudaSuccess)
             return PGT_ERR_CUDA;
     }
 
-    const bool bmn = d.b_layout == PGT_B_KN;
-    CUtensorMap ta, tb, tc;
-    int rc = encode_tmap_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, d.K, d.M, d.lda * 2, 64, 128,
-                            CU_TENSOR_MAP_SWIZZLE_128B);
+    const CUtensorMapDataType op_type = mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int64_t es = mx ? 1 : 2;
+    const uint32_t bk = (uint32_t)s.bk;
+    const uint32_t bn_cta = (uint32_t)(s.bn / s.cs);
+    CUtensorMap ta, tb, tc, tsa, tsb;
+    rc = encode_tmap_2d(&ta, op_type, A, d.K, d.M, d.lda * es, bk, 128, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
     if (bmn)
-        rc = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, d.N, d.K, d.ldb * 2, 64, 64,
-                            CU_TENSOR_MAP_SWIZZLE_128B);
+        rc = encode_tmap_2d(&tb, op_type, B, d.N, d.K, d.ldb * es, 64, bk, CU_TENSOR_MAP_SWIZZLE_128B);
     else
-        rc = encode_tmap_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, d.K, d.N, d.ldb * 2, 64, plan.bn,
-                            CU_TENSOR_MAP_SWIZZLE_128B);
+        rc = encode_tmap_2d(&tb, op_type, B, d.K, d.N, d.ldb * es, bk, bn_cta, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
     rc = encode_tmap_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, C, d.N, d.M, d.ldc * 2, 64, 32,
                         CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
+    tsa = ta;
+    tsb = ta;
+    if (mx) {
+        const SfGeometry sg = sf_geometry(d.M, d.N, d.K);
+        uint32_t* wa = static_cast<uint32_t*>(workspace);
+        uint32_t* wb = wa + sg.bytes_a / 4;
+        const int64_t words = (int64_t)(sg.bytes_a + sg.bytes_b) / 4;
+        int blocks = (int)((words + 255) / 256);
+        if (blocks > 4 * ctx->num_sms) blocks = 4 * ctx->num_sms;
+        sf_repack_kernel<<<blocks, 256, 0, stream>>>(sfa, sfb, (int)d.M, (int)d.N, sg.kb, sg.kgroups, sg.ma, sg.nb,
+                                                     wa, wb);
+        if (cudaGetLastError() != cudaSuccess) return PGT_ERR_CUDA;
+        rc = encode_tmap_2d(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT32, wa, 128, (uint64_t)sg.kgroups * sg.ma, 512, 128, 1,
+                            CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (rc) return rc;
+        rc = encode_tmap_2d(&tsb, CU_TENSOR_MAP_DATA_TYPE_UINT32, wb, 128, (uint64_t)sg.kgroups * sg.nb, 512, 128,
+                            (uint32_t)((s.bn + 127) / 128), CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (rc) return rc;
+        gp.sfa_rows = sg.ma;
+        gp.sfb_rows = sg.nb;
+    }
 
-    const bool tr = trace != nullptr;
-    if (plan.kernel_cfg == PGT_CFG_1CTA_128x256)
-        return dispatch_bf16_1cta<256, 4>(bmn, tr, ta, tb, tc, gp, plan.ctas, ctx->device, stream);
-    if (plan.kernel_cfg == PGT_CFG_1CTA_128x128)
-        return dispatch_bf16_1cta<128, 6>(bmn, tr, ta, tb, tc, gp, plan.ctas, ctx->device, stream);
-    return PGT_ERR_UNSUPPORTED;
+    KernelFn k = pick_kernel(plan.kernel_cfg, mx, bmn, tr);
+    if (k == nullptr) return PGT_ERR_UNSUPPORTED;
+    cudaLaunchConfig_t lc = {};
+    cudaLaunchAttribute at[1];
+    lc.gridDim = dim3(plan.ctas, 1, 1);
+    lc.blockDim = dim3(kThreads, 1, 1);
+    lc.dynamicSmemBytes = s.smem;
+    lc.stream = stream;
+    if (s.cs > 1) {
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = s.cs;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        lc.attrs = at;
+        lc.numAttrs = 1;
+    }
+    if (cudaLaunchKernelEx(&lc, k, ta, tb, tc, tsa, tsb, gp) != cudaSuccess) {
+        cudaGetLastError();
+        return PGT_ERR_CUDA;
+    }
+    return PGT_OK;
 }
 
 }  // namespace pgt

@@ -18,7 +18,7 @@ from oracle import schedule as S
 pytestmark = pytest.mark.gpu
 
 ALL_MODES = [pgt.BLOCKED, pgt.INTERLEAVED, pgt.SWIZZLED, pgt.WORK_STEALING, pgt.BLOCKED_GROUPED_M]
-BF16_CFGS = [pgt.CFG_1CTA_128x128, pgt.CFG_1CTA_128x256]
+BF16_CFGS = [pgt.CFG_1CTA_128x128, pgt.CFG_1CTA_128x256, pgt.CFG_2CTA_256x128, pgt.CFG_2CTA_256x256]
 
 
 @pytest.fixture(scope="module")
@@ -110,6 +110,17 @@ def plan_ws(ctx):
     return min(8, ctx.max_groups)
 
 
+def worker_visits(visits, cs):
+    """Per-worker visit lists from per-CTA traces; both CTAs of a pair must agree."""
+    out = []
+    for w in range(len(visits) // cs):
+        lists = [[(t, m, n) for (t, m, n, _) in v] for v in visits[w * cs:(w + 1) * cs]]
+        for other in lists[1:]:
+            assert other == lists[0], f"CTAs of pair {w} visited different tiles"
+        out.append(visits[w * cs])
+    return out
+
+
 # ------------------------------------------------------------- K tails, layouts
 @pytest.mark.parametrize("cfg", BF16_CFGS)
 @pytest.mark.parametrize("K", [1, 63, 64, 65, 130, 1000])
@@ -155,7 +166,9 @@ def test_modes_bit_identical_with_traces(ctx, cfg, workers):
             else:
                 assert np.array_equal(c, ref), (mode, G)
             visits, _ = tb.read()
-            grid = S.Grid(plan["m_blocks"], plan["n_blocks"], 1)
+            cs = plan["cluster_size"]
+            visits = worker_visits(visits, cs)
+            grid = S.Grid(plan["m_blocks"], plan["n_blocks"], cs)
             if mode == pgt.WORK_STEALING:
                 S.check_ws_trace([[t for (t, _, _, _) in v] for v in visits], grid.tiles, 4)
             else:
@@ -173,14 +186,15 @@ def ragged_inputs():
     return synthetic.gemm_bf16_sequence(RAGGED, seed=3, dist="uniform")
 
 
+@pytest.mark.parametrize("cfg", [pgt.CFG_1CTA_128x256, pgt.CFG_2CTA_256x128])
 @pytest.mark.parametrize("idx", [0, 1, 2])
-def test_ragged_set_all_modes(ctx, ragged_inputs, idx):
+def test_ragged_set_all_modes(ctx, ragged_inputs, idx, cfg):
     M, N, K = RAGGED[idx]
     A, B = ragged_inputs[idx]
     dA, dB = dev_u16(A), dev_u16(B)
     ref = None
     for mode in ALL_MODES:
-        C, plan, _ = run(ctx, dA, dB, M, N, K, mode=mode, G=16)
+        C, plan, _ = run(ctx, dA, dB, M, N, K, mode=mode, G=16, cfg=cfg)
         if ref is None:
             ref = C
             rows = sample_rows(M, plan["bm"], 24, seed=idx)
@@ -199,12 +213,13 @@ def big_inputs():
     return A, B
 
 
-def test_8192_swizzled_vs_work_stealing(ctx, big_inputs):
+@pytest.mark.parametrize("cfg", [pgt.CFG_AUTO, pgt.CFG_2CTA_256x128, pgt.CFG_2CTA_256x256])
+def test_8192_swizzled_vs_work_stealing(ctx, big_inputs, cfg):
     M = N = K = 8192
     A, B = big_inputs
     dA, dB = dev_u16(A), dev_u16(B)
-    C1, plan, _ = run(ctx, dA, dB, M, N, K, mode=pgt.SWIZZLED, G=16)
-    C2, _, _ = run(ctx, dA, dB, M, N, K, mode=pgt.WORK_STEALING, G=16)
+    C1, plan, _ = run(ctx, dA, dB, M, N, K, mode=pgt.SWIZZLED, G=16, cfg=cfg)
+    C2, _, _ = run(ctx, dA, dB, M, N, K, mode=pgt.WORK_STEALING, G=16, cfg=cfg)
     assert torch.equal(C1, C2)
     rows = sample_rows(M, plan["bm"], 26, seed=2)
     C64, Abs = OG.gemm_rows(OG.dequant_bf16(A), OG.dequant_bf16(B), True, K, N, rows)
@@ -223,6 +238,7 @@ def test_argument_errors(ctx):
         (dict(group_size=0), pgt.ERR_ARG),
         (dict(sched_mode=9), pgt.ERR_ARG),
         (dict(kernel_cfg=pgt.CFG_2CTA_256x256 + 1), pgt.ERR_UNSUPPORTED),
+        (dict(dtype=pgt.MXFP8, b_layout=pgt.B_KN), pgt.ERR_ARG),  # MXFP8 needs B stored N x K
     ]
     for kw, status in bad:
         args = dict(M=64, N=64, K=64)
