@@ -339,6 +339,15 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
         tf = FLOP / (ms * 1e-3) / 1e12
         per_mode[name] = {"tflops": tf, "ms": ms, "frac_of_burst_peak": tf / peaks["bf16_burst"]}
     out["per_mode"] = per_mode
+    # work stealing with 1..16 counter groups
+    ws_sweep = {}
+    for g in (1, 2, 4, 8, 16):
+        d = pgt.make_desc(M, N, K, b_layout=pgt.B_KN, sched_mode=pgt.WORK_STEALING, group_size=16, ws_groups=g,
+                          kernel_cfg=args.cfg)
+        _, per = time_launches(torch, lambda: ctx.gemm_ex(d, dA, dB, dC), 40, 5)
+        ms = float(np.median(per))
+        ws_sweep[f"groups_{g}"] = {"tflops": FLOP / (ms * 1e-3) / 1e12, "ms": ms}
+    out["work_stealing_groups"] = ws_sweep
     # per kernel configuration (swizzled, group 16)
     per_cfg = {}
     for cfg, cname in ((pgt.CFG_1CTA_128x128, "1cta_128x128"), (pgt.CFG_1CTA_128x256, "1cta_128x256"),
