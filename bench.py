@@ -34,6 +34,30 @@ WORKLOAD = "bf16 GEMM M=N=K=8192, A,B ~ N(0,1)/sqrt(K) seed 2, B stored KxN, swi
 L2_NOTE = "inputs larger than L2: A+B+C = 384 MiB per GEMM > 129 MB L2; add x+y+out = 768 MiB"
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture
+# of each kernel (summaries under profiles/).  A figure is reported only while the kernel's
+# sources hash to the fingerprint taken with it; after any change the roofline says null.
+GEMM_SOURCES = ["csrc/pgt_gemm.cu", "csrc/pgt_device.cuh", "csrc/pgt_sched.cuh"]
+ADD_SOURCES = ["csrc/pgt_add.cu", "csrc/pgt_device.cuh", "csrc/pgt_sched.cuh"]
+PROFILED_TRAFFIC = {
+    "gemm_bf16_2cta_256x256": (1.240241e9 + 1.28645376e8, GEMM_SOURCES, "1e09cd9d3fabe562"),
+    "gemm_mxfp8_2cta_256x256": (2.48906496e8 + 1.16763136e8, GEMM_SOURCES, "1e09cd9d3fabe562"),
+    "add_wide_8x1024": (5.36910592e8 + 2.29790976e8, ADD_SOURCES, "0ec4cdbf39d2f292"),
+}
+
+
+def profiled_traffic(key: str):
+    import hashlib
+    if key not in PROFILED_TRAFFIC:
+        return None
+    nbytes, files, fingerprint = PROFILED_TRAFFIC[key]
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "persistent_gemm_tile_gb300", f), "rb") as fh:
+            h.update(fh.read())
+    return nbytes if h.hexdigest()[:16] == fingerprint else None
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -41,8 +65,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cfg", type=int, default=0, help="kernel configuration (PGT_CFG_*), 0 = auto")
-    ap.add_argument("--kernel", default="gemm", choices=["gemm", "add"],
-                    help="headline kernel: the GEMM (default) or the persistent add (for profiling the add)")
+    ap.add_argument("--kernel", default="gemm", choices=["gemm", "add", "mxfp8"],
+                    help="headline kernel: the bf16 GEMM (default), or the persistent add / the MXFP8 GEMM "
+                         "(for timing and profiling those kernels alone)")
     ap.add_argument("--no-extras", action="store_true", help="headline only")
     ap.add_argument("--ragged", action="store_true",
                     help="also time the ragged-tail GEMM set per scheduler, with tail idle from traces")
@@ -248,6 +273,8 @@ def run_ours(args, world, rank, local, pg):
     launch = lambda: ctx.gemm_ex(head, dA, dB, dC)  # noqa: E731
     if args.kernel == "add":
         return run_add_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peaks)
+    if args.kernel == "mxfp8":
+        return run_mx_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peaks, dC)
 
     # ------------------------------------------------------------------ headline
     for _ in range(args.warmup):
@@ -279,7 +306,8 @@ def run_ours(args, world, rank, local, pg):
                    "ctas_per_worker": plan["cluster_size"], "workers": plan["workers"], "stages": plan["stages"],
                    "l2": L2_NOTE, "parallelism": f"{world} independent GEMMs (one per GPU)"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": profiled_traffic("gemm_bf16_2cta_256x256") if plan["kernel_cfg"] == 4 else None,
                      "peak_kind": ("sustained" if long_region else "burst") + f" bf16 ({peaks['source']})"},
         "gpu_launches": args.steps,
         "clocks": clk,
@@ -324,17 +352,62 @@ def run_add_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peak
     ctx.close()
 
 
+def run_mx_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peaks, dC):
+    """The MXFP8 GEMM 8192^3 (2 launches per step: scale repack + GEMM) as the timed kernel."""
+    import synthetic
+    qa, sa, qb, sb = synthetic.gemm_mxfp8_inputs(M, N, K, seed=4)
+    tqa, tsa = torch.from_numpy(qa).to(device), torch.from_numpy(sa).to(device)
+    tqb, tsb = torch.from_numpy(qb).to(device), torch.from_numpy(sb).to(device)
+    d = pgt.make_desc(M, N, K, dtype=pgt.MXFP8, b_layout=pgt.B_NK, sched_mode=pgt.SWIZZLED, group_size=16,
+                      kernel_cfg=args.cfg)
+    plan = ctx.gemm_plan(d)
+    ws = torch.empty(ctx.gemm_workspace_bytes(d), dtype=torch.uint8, device=device)
+    launch = lambda: ctx.gemm_ex(d, tqa, tqb, dC, sfa=tsa, sfb=tsb, workspace=ws)  # noqa: E731
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize()
+    barrier(pg)
+    clocks = Clocks(local)
+    clocks.start()
+    total_ms, per = time_launches(torch, launch, args.steps, 0)
+    clk = clocks.stop()
+    barrier(pg)
+    total_ms = max_over_ranks(pg, total_ms, device)
+    kern_ms = float(np.mean(per))
+    achieved = FLOP / (kern_ms * 1e-3) / 1e12
+    fp8_peak = 2.0 * peaks["bf16_burst"]
+    out = {"metric": "MXFP8 GEMM TFLOP/s vs fp8 tensor peak", "value": world * FLOP * args.steps / (total_ms * 1e-3) / 1e12,
+           "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": "e4m3+e8m0", "data": "synthetic",
+           "config": {"workload": "MXFP8 8192^3 seed 4, swizzled group 16", "kernel_cfg": plan["kernel_cfg"],
+                      "tile": f"{plan['bm'] * plan['cluster_size']}x{plan['bn']}", "l2": L2_NOTE},
+           "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                        "frac": achieved / fp8_peak, "traffic": None,
+                        "peak_kind": f"2 x bf16 burst ({peaks['source']})"},
+           "gpu_launches": 2 * args.steps, "clocks": clk}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    ctx.close()
+
+
 def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
     import synthetic
     A_host = dA.cpu().numpy().view(np.uint16)
     B_host = dB.cpu().numpy().view(np.uint16)
-    # per scheduler mode
+    # per scheduler mode: rounds of 10 launches per mode, modes interleaved so that each sees
+    # the same mix of power and clock states; median per-launch time
     per_mode = {}
     names = {pgt.BLOCKED: "blocked", pgt.INTERLEAVED: "interleaved", pgt.SWIZZLED: "swizzled",
              pgt.WORK_STEALING: "work_stealing", pgt.BLOCKED_GROUPED_M: "blocked_grouped_m"}
-    for mode, name in names.items():
-        d = desc_for(mode)
-        _, per = time_launches(torch, lambda: ctx.gemm_ex(d, dA, dB, dC), 40, 5)
+    samples = {name: [] for name in names.values()}
+    descs = {mode: desc_for(mode) for mode in names}
+    for _ in range(6):
+        for mode, name in names.items():
+            d = descs[mode]
+            _, per = time_launches(torch, lambda: ctx.gemm_ex(d, dA, dB, dC), 10, 2)
+            samples[name].extend(per)
+    for name, per in samples.items():
         ms = float(np.median(per))
         tf = FLOP / (ms * 1e-3) / 1e12
         per_mode[name] = {"tflops": tf, "ms": ms, "frac_of_burst_peak": tf / peaks["bf16_burst"]}
@@ -348,12 +421,18 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
         ms = float(np.median(per))
         ws_sweep[f"groups_{g}"] = {"tflops": FLOP / (ms * 1e-3) / 1e12, "ms": ms}
     out["work_stealing_groups"] = ws_sweep
-    # per kernel configuration (swizzled, group 16)
+    # per kernel configuration (swizzled, group 16), interleaved the same way
     per_cfg = {}
-    for cfg, cname in ((pgt.CFG_1CTA_128x128, "1cta_128x128"), (pgt.CFG_1CTA_128x256, "1cta_128x256"),
-                       (pgt.CFG_2CTA_256x128, "2cta_256x128"), (pgt.CFG_2CTA_256x256, "2cta_256x256")):
-        d = desc_for(pgt.SWIZZLED, cfg)
-        _, per = time_launches(torch, lambda: ctx.gemm_ex(d, dA, dB, dC), 40, 5)
+    cfgs = ((pgt.CFG_1CTA_128x128, "1cta_128x128"), (pgt.CFG_1CTA_128x256, "1cta_128x256"),
+            (pgt.CFG_2CTA_256x128, "2cta_256x128"), (pgt.CFG_2CTA_256x256, "2cta_256x256"))
+    csamples = {cname: [] for _, cname in cfgs}
+    cdescs = {cname: desc_for(pgt.SWIZZLED, cfg) for cfg, cname in cfgs}
+    for _ in range(4):
+        for _, cname in cfgs:
+            d = cdescs[cname]
+            _, per = time_launches(torch, lambda: ctx.gemm_ex(d, dA, dB, dC), 10, 2)
+            csamples[cname].extend(per)
+    for cname, per in csamples.items():
         ms = float(np.median(per))
         per_cfg[cname] = {"tflops": FLOP / (ms * 1e-3) / 1e12, "ms": ms}
     out["per_cfg"] = per_cfg
@@ -383,7 +462,9 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
             if best is None or gbs > best[1]:
                 best = (f"{tname}_{mname}", gbs, ms)
     add["roofline"] = {"bound": "hbm", "achieved": best[1], "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                       "frac": best[1] / peaks["hbm_gbs"], "traffic": None, "kernel": best[0],
+                       "frac": best[1] / peaks["hbm_gbs"],
+                       "traffic": profiled_traffic("add_wide_8x1024") if best[0].startswith("wide") else None,
+                       "kernel": best[0],
                        "algorithmic_bytes": ADD_BYTES}
     add["workload"] = "fp32 8192x8192 x,y ~ N(0,1) seed 1, out = x + y"
     out["add"] = add
@@ -405,7 +486,9 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
         mx[cname] = {"tflops": tf, "ms": ms, "frac_of_fp8_peak": tf / fp8_peak}
     best = max(mx, key=lambda k: mx[k]["tflops"])
     mx["roofline"] = {"bound": "tensor", "achieved": mx[best]["tflops"], "peak": fp8_peak, "unit": "TFLOP/s",
-                      "frac": mx[best]["tflops"] / fp8_peak, "traffic": None, "kernel": best,
+                      "frac": mx[best]["tflops"] / fp8_peak,
+                      "traffic": profiled_traffic("gemm_mxfp8_2cta_256x256") if best == "2cta_256x256" else None,
+                      "kernel": best,
                       "peak_kind": f"2 x measured bf16 burst ({peaks['source']}), nominal fp8/bf16 ratio"}
     mx["workload"] = "MXFP8 8192^3, E4M3 payload N(0,1), E8M0 per 1x128 K block, exps U{-4..4}, seed 4, " \
                      "swizzled group 16; time includes the per-call scale repack"

@@ -1,0 +1,61 @@
+"""The benchmark's multi-rank logic on CPU: two gloo ranks on 127.0.0.1.
+
+The GEMM shards into independent problems, one per GPU, so the only cross-rank steps are the
+barrier around the timed region and the max over ranks of its duration; the reference arm
+runs on rank 0 alone and prints exactly one JSON line."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+
+    class Args:
+        impl = "reference"
+
+    w, r, local, pg = bench.dist_setup(Args)
+    assert (w, r) == (world, rank) and pg is not None
+    bench.barrier(pg)
+    got = bench.max_over_ranks(pg, 10.0 + rank, "cpu")
+    out[rank] = got
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_barrier_two_gloo_ranks():
+    port = _free_port()
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
+        assert dict(out) == {0: 11.0, 1: 11.0}
+
+
+def test_reference_arm_under_torchrun_prints_one_line_from_rank0():
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "0"]
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
+    assert rec["e2e"]["h2d_bytes_per_step"] == 0 and rec["cpu_baseline"]["kind"] == "oracle"
