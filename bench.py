@@ -421,6 +421,16 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
         ms = float(np.median(per))
         ws_sweep[f"groups_{g}"] = {"tflops": FLOP / (ms * 1e-3) / 1e12, "ms": ms}
     out["work_stealing_groups"] = ws_sweep
+    # swizzle group width (column blocks per group), interleaved rounds
+    gsamples = {g: [] for g in (2, 4, 8, 16, 32)}
+    gdescs = {g: pgt.make_desc(M, N, K, b_layout=pgt.B_KN, sched_mode=pgt.SWIZZLED, group_size=g,
+                               kernel_cfg=args.cfg) for g in gsamples}
+    for _ in range(4):
+        for g, d in gdescs.items():
+            _, per = time_launches(torch, lambda: ctx.gemm_ex(d, dA, dB, dC), 10, 2)
+            gsamples[g].extend(per)
+    out["swizzle_groups"] = {f"group_{g}": {"tflops": FLOP / (float(np.median(v)) * 1e-3) / 1e12,
+                                            "ms": float(np.median(v))} for g, v in gsamples.items()}
     # per kernel configuration (swizzled, group 16), interleaved the same way
     per_cfg = {}
     cfgs = ((pgt.CFG_1CTA_128x128, "1cta_128x128"), (pgt.CFG_1CTA_128x256, "1cta_128x256"),

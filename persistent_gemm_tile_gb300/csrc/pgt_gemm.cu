@@ -367,18 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row0 = (e.y * CS + (int)rank) * L::BM + 32 * qw;
             const int col0 = e.z * BN;
             const uint32_t tacc = tmem_base + ((uint32_t)(32 * qw) << 16) + acc * BN;
-#pragma unroll 1
-            for (int c = 0; c < BN / 64; ++c, ++chunk) {
-                uint32_t r0[32], r1[32];
-                tmem_ld_32x32b_x32(tacc + c * 64, r0);
-                tmem_ld_32x32b_x32(tacc + c * 64 + 32, r1);
-                tmem_ld_wait();
-                if (c == BN / 64 - 1) {
-                    // accumulator fully read: hand it back to the MMA warp
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) arrive_local_or_leader(tempty(acc), !leader);
-                }
+            // Stage 64 columns (32 packed bf16 pairs per row) in this warp's 128B-swizzled
+            // buffer and store them with one TMA box; edges are clipped by the tensor map.
+            auto store_chunk = [&](int c, const uint32_t* w) __attribute__((always_inline)) {
                 const uint32_t buf = epi + (chunk % L::EPI_BUFS) * kEpiBufBytes;
                 if (lane == 0) {
                     if constexpr (L::EPI_BUFS == 2)
@@ -389,23 +380,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 const uint32_t rowaddr = buf + lane * 128u;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    st_shared_v4(rowaddr + ((j ^ (lane & 7u)) << 4), pack_bf16x2(r0[8 * j], r0[8 * j + 1]),
-                                 pack_bf16x2(r0[8 * j + 2], r0[8 * j + 3]), pack_bf16x2(r0[8 * j + 4], r0[8 * j + 5]),
-                                 pack_bf16x2(r0[8 * j + 6], r0[8 * j + 7]));
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    st_shared_v4(rowaddr + (((j + 4) ^ (lane & 7u)) << 4), pack_bf16x2(r1[8 * j], r1[8 * j + 1]),
-                                 pack_bf16x2(r1[8 * j + 2], r1[8 * j + 3]), pack_bf16x2(r1[8 * j + 4], r1[8 * j + 5]),
-                                 pack_bf16x2(r1[8 * j + 6], r1[8 * j + 7]));
-                }
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(rowaddr + ((j ^ (lane & 7u)) << 4), w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
                     const int x = col0 + 64 * c;
                     if (row0 < gp.M && x < gp.N) tma_store_2d(&tmC, buf, x, row0);
                     bulk_commit();
+                }
+                ++chunk;
+            };
+            if constexpr (L::ACC_BUFS == 1) {
+                // a single accumulator: read all of it into registers (as bf16 pairs), hand
+                // it back to the MMA warp at once, then stage and store
+                uint32_t pk[BN / 2];
+#pragma unroll
+                for (int c = 0; c < BN / 64; ++c) {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld_32x32b_x32(tacc + c * 64, r0);
+                    tmem_ld_32x32b_x32(tacc + c * 64 + 32, r1);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        pk[32 * c + i] = pack_bf16x2(r0[2 * i], r0[2 * i + 1]);
+                        pk[32 * c + 16 + i] = pack_bf16x2(r1[2 * i], r1[2 * i + 1]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) arrive_local_or_leader(tempty(acc), !leader);
+#pragma unroll
+                for (int c = 0; c < BN / 64; ++c) store_chunk(c, pk + 32 * c);
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < BN / 64; ++c) {
+                    uint32_t r0[32], r1[32], w[32];
+                    tmem_ld_32x32b_x32(tacc + c * 64, r0);
+                    tmem_ld_32x32b_x32(tacc + c * 64 + 32, r1);
+                    tmem_ld_wait();
+                    if (c == BN / 64 - 1) {
+                        // accumulator fully read: hand it back to the MMA warp
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) arrive_local_or_leader(tempty(acc), !leader);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        w[i] = pack_bf16x2(r0[2 * i], r0[2 * i + 1]);
+                        w[16 + i] = pack_bf16x2(r1[2 * i], r1[2 * i + 1]);
+                    }
+                    store_chunk(c, w);
                 }
             }
             ++tc;
