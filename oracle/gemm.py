@@ -17,6 +17,13 @@ Checks (the bar these kernels are held to):
   is taken against the bf16-rounded result, because bf16 output rounding alone already
   gives ~1.5e-3 relative Frobenius error against the unrounded fp64 product.
 * (ii) per element ``|C - C64| <= 1e-2 * Abs64`` against the unrounded product.
+
+Epilogue extension (tritonBLAS "Work Stealing Scheduler Kernel", the matmul hunk passes
+``a_scale`` / ``b_scale`` "if quantized" and a bias marked TODO; their semantics are not on
+the page).  Reading: per-tensor scales fold into one factor ``alpha = a_scale * b_scale`` and
+the bias is one value per output column, so ``C = alpha * (A . B) + bias[n]``.  The bars
+become: Frobenius against ``bf16_rne(alpha * C64 + bias)`` and, per element,
+``|C - (alpha * C64 + bias)| <= 1e-2 * (|alpha| * Abs64 + |bias|)``.
 """
 from __future__ import annotations
 
@@ -118,6 +125,17 @@ def gemm_entries(A64, B64, b_kn: bool, K: int, ii, jj) -> tuple[np.ndarray, np.n
 
 
 # ------------------------------------------------------------------------------ checks
+def epilogue(C64, Abs64, alpha: float = 1.0, bias=None):
+    """Apply ``C = alpha * C + bias[n]`` to the fp64 product and its error bound."""
+    C = float(alpha) * np.asarray(C64, dtype=np.float64)
+    A = abs(float(alpha)) * np.asarray(Abs64, dtype=np.float64)
+    if bias is not None:
+        b = np.asarray(bias, dtype=np.float64)[None, :]
+        C = C + b
+        A = A + np.abs(b)
+    return C, A
+
+
 def check(C_bits, C64, Abs64, frob_tol: float = FROB_TOL, elem_tol: float = ELEM_TOL) -> dict:
     """Compare bf16 results (uint16 bits) with the fp64 oracle; raises AssertionError."""
     Cg = numerics.bf16_bits_to_f64(C_bits)

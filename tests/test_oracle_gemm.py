@@ -134,3 +134,32 @@ def test_checker_accepts_rounded_result_and_rejects_planted_errors():
     with pytest.raises(AssertionError):  # a dropped K block
         C_drop, _ = G.gemm_full(A[:, :192], B[:192], True, 64, 64, 192)
         G.check(nm.f64_to_bf16_rne(C_drop), C64, Abs)
+
+
+def test_epilogue_identity_and_closed_form():
+    rng = np.random.default_rng(8)
+    C64 = rng.standard_normal((5, 7))
+    Abs = np.abs(C64) + 1.0
+    C1, A1 = G.epilogue(C64, Abs)
+    assert np.array_equal(C1, C64) and np.array_equal(A1, Abs)
+    # all-ones operands: C = alpha * K + bias[n], exact
+    K = 256
+    C, Ab = G.gemm_full(np.ones((3, K)), np.ones((K, 4)), True, 3, 4, K)
+    bias = np.array([0.5, -1.0, 2.0, 0.0])
+    Ce, Ae = G.epilogue(C, Ab, alpha=0.25, bias=bias)
+    assert np.array_equal(Ce, np.tile(0.25 * K + bias, (3, 1)))
+    assert np.array_equal(Ae, np.tile(0.25 * K + np.abs(bias), (3, 1)))
+
+
+def test_epilogue_checker_rejects_missing_bias_or_scale():
+    rng = np.random.default_rng(9)
+    A = _bf16(rng.uniform(-1, 1, (32, 128)))
+    B = _bf16(rng.uniform(-1, 1, (128, 48)))
+    C64, Abs = G.gemm_full(A, B, True, 32, 48, 128)
+    bias = rng.uniform(-4, 4, 48)
+    Ce, Ae = G.epilogue(C64, Abs, alpha=-1.5, bias=bias)
+    G.check(nm.f64_to_bf16_rne(Ce), Ce, Ae)
+    with pytest.raises(AssertionError):  # bias dropped
+        G.check(nm.f64_to_bf16_rne(-1.5 * C64), Ce, Ae)
+    with pytest.raises(AssertionError):  # scale dropped
+        G.check(nm.f64_to_bf16_rne(C64 + bias[None, :]), Ce, Ae)
