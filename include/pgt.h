@@ -92,6 +92,13 @@ extern "C" {
 #define PGT_CFG_2CTA_256x128 3
 #define PGT_CFG_2CTA_256x256 4
 
+/* Epilogue options ([WS] passes a_scale / b_scale "if quantized" and marks bias TODO).
+ * Reading taken here: per-tensor scales fold into one factor alpha = a_scale * b_scale and
+ * the bias is one fp32 value per output column, so C = alpha * (A . B) + bias[n], computed
+ * in fp32 (one fused multiply-add per element) before the bf16 rounding. */
+#define PGT_EPI_ALPHA 1
+#define PGT_EPI_BIAS 2
+
 /* pgt_preamble flags */
 #define PGT_FLAG_HOST_RESET 1 /* reset work-stealing counters with a memset before every
                                  launch ([WS] reset_tile_counter) instead of in-kernel */
@@ -114,7 +121,10 @@ typedef struct pgt_gemm_desc {
     int32_t ws_groups;   /* work-stealing counter groups, 1 .. max_groups (0 = min(8, max)) */
     int32_t kernel_cfg;  /* PGT_CFG_* */
     int32_t num_workers; /* persistent workers; 0 = one per SM (pair), capped at T */
+    int32_t epilogue;    /* 0, or PGT_EPI_ALPHA | PGT_EPI_BIAS */
+    float alpha;         /* with PGT_EPI_ALPHA: C = alpha * (A . B) [+ bias] */
     int32_t reserved;
+    const float* bias;   /* with PGT_EPI_BIAS: DEVICE fp32[N], added to every row of C */
 } pgt_gemm_desc;
 
 /* What a GEMM launch will do; filled by pgt_gemm_plan. */

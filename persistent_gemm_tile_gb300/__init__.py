@@ -26,6 +26,7 @@ SCHED = {"blocked": BLOCKED, "interleaved": INTERLEAVED, "swizzled": SWIZZLED,
          "work_stealing": WORK_STEALING, "blocked_grouped_m": BLOCKED_GROUPED_M}
 CFG_AUTO, CFG_1CTA_128x128, CFG_1CTA_128x256, CFG_2CTA_256x128, CFG_2CTA_256x256 = 0, 1, 2, 3, 4
 FLAG_HOST_RESET = 1
+EPI_ALPHA, EPI_BIAS = 1, 2
 VISIT_FIELDS = 4
 
 # every symbol include/pgt.h declares
@@ -42,7 +43,8 @@ class GemmDesc(ctypes.Structure):
                 ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldc", ctypes.c_int64),
                 ("dtype", ctypes.c_int32), ("b_layout", ctypes.c_int32), ("sched_mode", ctypes.c_int32),
                 ("group_size", ctypes.c_int32), ("ws_groups", ctypes.c_int32), ("kernel_cfg", ctypes.c_int32),
-                ("num_workers", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("num_workers", ctypes.c_int32), ("epilogue", ctypes.c_int32), ("alpha", ctypes.c_float),
+                ("reserved", ctypes.c_int32), ("bias", ctypes.c_void_p)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -128,11 +130,16 @@ def _stream(stream) -> int | None:
 
 
 def make_desc(M, N, K, *, lda=0, ldb=0, ldc=0, dtype=BF16, b_layout=B_KN, sched_mode=SWIZZLED,
-              group_size=16, ws_groups=0, kernel_cfg=CFG_AUTO, num_workers=0) -> GemmDesc:
+              group_size=16, ws_groups=0, kernel_cfg=CFG_AUTO, num_workers=0, alpha=None, bias=None) -> GemmDesc:
+    """A pgt_gemm_desc; alpha (a_scale * b_scale) and bias (device fp32[N]) enable the epilogue.
+
+    The descriptor stores only the bias tensor's address: keep the tensor alive until the
+    GEMMs that use this descriptor have finished."""
     if isinstance(sched_mode, str):
         sched_mode = SCHED[sched_mode]
+    epi = (EPI_ALPHA if alpha is not None else 0) | (EPI_BIAS if bias is not None else 0)
     return GemmDesc(M, N, K, lda, ldb, ldc, dtype, b_layout, sched_mode, group_size, ws_groups, kernel_cfg,
-                    num_workers, 0)
+                    num_workers, epi, 1.0 if alpha is None else float(alpha), 0, _ptr(bias))
 
 
 def gemm_noalloc(A, B, C, M, N, K, b_layout=B_KN, group_size=16, ws_groups=0, err=None, stream=None) -> None:

@@ -35,6 +35,9 @@ struct GemmParams {
     int* err;
     int sfa_rows;  // MXFP8: rows of 128-row scale blocks per k group in the packed SFA
     int sfb_rows;  // MXFP8: same for SFB
+    int epi;       // nonzero: C = alpha * acc + bias[n] before rounding
+    float alpha;
+    const float* bias;  // fp32[N] or nullptr
     int32_t* tr_visits;
     int64_t tr_max;
     int32_t* tr_counts;
@@ -367,6 +370,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row0 = (e.y * CS + (int)rank) * L::BM + 32 * qw;
             const int col0 = e.z * BN;
             const uint32_t tacc = tmem_base + ((uint32_t)(32 * qw) << 16) + acc * BN;
+            // fp32 accumulator pair -> bf16x2, with the optional scale and bias fused in
+            // (one fma per element; columns past N read no bias)
+            auto cvt = [&](uint32_t lo, uint32_t hi, int col) __attribute__((always_inline)) -> uint32_t {
+                if (!gp.epi) return pack_bf16x2(lo, hi);
+                float b0 = 0.f, b1 = 0.f;
+                if (gp.bias != nullptr) {
+                    if (col < gp.N) b0 = __ldg(gp.bias + col);
+                    if (col + 1 < gp.N) b1 = __ldg(gp.bias + col + 1);
+                }
+                const float v0 = __fmaf_rn(gp.alpha, __uint_as_float(lo), b0);
+                const float v1 = __fmaf_rn(gp.alpha, __uint_as_float(hi), b1);
+                return pack_bf16x2(__float_as_uint(v0), __float_as_uint(v1));
+            };
             // Stage 64 columns (32 packed bf16 pairs per row) in this warp's 128B-swizzled
             // buffer and store them with one TMA box; edges are clipped by the tensor map.
             auto store_chunk = [&](int c, const uint32_t* w) __attribute__((always_inline)) {
@@ -403,8 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        pk[32 * c + i] = pack_bf16x2(r0[2 * i], r0[2 * i + 1]);
-                        pk[32 * c + 16 + i] = pack_bf16x2(r1[2 * i], r1[2 * i + 1]);
+                        pk[32 * c + i] = cvt(r0[2 * i], r0[2 * i + 1], col0 + 64 * c + 2 * i);
+                        pk[32 * c + 16 + i] = cvt(r1[2 * i], r1[2 * i + 1], col0 + 64 * c + 32 + 2 * i);
                     }
                 }
                 tc_fence_before();
@@ -427,8 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        w[i] = pack_bf16x2(r0[2 * i], r0[2 * i + 1]);
-                        w[16 + i] = pack_bf16x2(r1[2 * i], r1[2 * i + 1]);
+                        w[i] = cvt(r0[2 * i], r0[2 * i + 1], col0 + 64 * c + 2 * i);
+                        w[16 + i] = cvt(r1[2 * i], r1[2 * i + 1], col0 + 64 * c + 32 + 2 * i);
                     }
                     store_chunk(c, w);
                 }
@@ -728,6 +744,9 @@ int gemm_launch(pgt_ctx* ctx, const pgt_gemm_desc& d, const pgt_gemm_plan_info& 
     if (trace != nullptr) {
         if (trace->visits == nullptr || trace->counts == nullptr || trace->max_visits < 1) return PGT_ERR_ARG;
     }
+    if (d.epilogue & ~(PGT_EPI_ALPHA | PGT_EPI_BIAS)) return PGT_ERR_ARG;
+    if ((d.epilogue & PGT_EPI_BIAS) && (d.bias == nullptr || (reinterpret_cast<uintptr_t>(d.bias) & 3u)))
+        return PGT_ERR_ARG;
     CfgShape s;
     if (!cfg_shape(plan.kernel_cfg, d.dtype, &s)) return PGT_ERR_UNSUPPORTED;
     const bool bmn = d.b_layout == PGT_B_KN;
@@ -759,6 +778,9 @@ int gemm_launch(pgt_ctx* ctx, const pgt_gemm_desc& d, const pgt_gemm_plan_info& 
     gp.err = ctx->d_err;
     gp.sfa_rows = 0;
     gp.sfb_rows = 0;
+    gp.epi = d.epilogue != 0;
+    gp.alpha = (d.epilogue & PGT_EPI_ALPHA) ? d.alpha : 1.0f;
+    gp.bias = (d.epilogue & PGT_EPI_BIAS) ? d.bias : nullptr;
     gp.tr_visits = trace ? trace->visits : nullptr;
     gp.tr_max = trace ? trace->max_visits : 0;
     gp.tr_counts = trace ? trace->counts : nullptr;
