@@ -206,3 +206,25 @@ def check_ws_trace(visits: list[list[int]], T: int, groups: int) -> None:
             if off == last_off:
                 assert t > last_t, f"worker {c} tickets not increasing in group {owner[t]}"
             last_off, last_t = off, t
+
+
+# --------------------------------------------------------------- fused multi-space loops
+def multi_space_schedule(mode: int, grids: list[Grid], P: int) -> list[list[tuple[int, int, int, int, int]]]:
+    """helion "Implement persistent kernels", the multi-loop listings: several independent
+    tile spaces share one id range; a worker's ids follow the blocked or interleaved order
+    over the total, and each id belongs to the first space whose range holds it, decoded
+    linearly (rows fastest) inside that space.  Per worker: (iter, tile_id, space, m, n)."""
+    firsts, total = [], 0
+    for g in grids:
+        firsts.append(total)
+        total += g.tiles
+    orders = order_blocked(total, P) if mode == BLOCKED else order_interleaved(total, P)
+    out = []
+    for tiles in orders:
+        visits = []
+        for i, t in enumerate(tiles):
+            s = max(k for k in range(len(grids)) if firsts[k] <= t)
+            m, n = decode_linear(t - firsts[s], grids[s].m_clusters)
+            visits.append((i, t, s, m, n))
+        out.append(visits)
+    return out

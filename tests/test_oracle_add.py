@@ -31,3 +31,16 @@ def test_add_exact_when_sum_is_representable():
     x = rng.integers(-2 ** 20, 2 ** 20, 1000).astype(np.float32)
     y = rng.integers(-2 ** 20, 2 ** 20, 1000).astype(np.float32)
     assert np.array_equal(add_f32(x, y), (x.astype(np.int64) + y.astype(np.int64)).astype(np.float32))
+
+
+def test_scale_exact_and_rounded():
+    from oracle.add import scale_f32
+    x = np.array([1.0, 2.0 ** -149, 3e38, 1.0 + 2.0 ** -23, -0.0], np.float32)
+    two = scale_f32(x, 2.0)
+    assert two[0] == 2.0 and two[1] == np.float32(2.0 ** -148) and np.isinf(two[2]) and np.signbit(two[4])
+    three = scale_f32(np.array([1.0 + 2.0 ** -23], np.float32), 3.0)
+    # 3 * (1 + 2^-23) = 3 + 1.5 ulp (ulp 2^-22 in [2, 4)): a tie between 3 + 2^-22 (odd) and 3 + 2^-21 (even)
+    assert three[0] == np.float32(3.0 + 2.0 ** -21)
+    rng = np.random.default_rng(1)
+    y = rng.standard_normal(1000).astype(np.float32)
+    assert np.array_equal(scale_f32(y, 3.0), (torch.from_numpy(y) * 3.0).numpy())

@@ -237,3 +237,33 @@ def test_ws_checker_rejects_planted_mistakes(plant):
             visits[0].append(t_g0)
     with pytest.raises(AssertionError):
         S.check_ws_trace(visits, 60, 3)
+
+
+# ------------------------------------------------------------------ multi-loop spaces
+def helion_multi_loop(total_x, nb0_x, nb0_y, pid):
+    """The multi-loop listing's per-pid branch, written literally."""
+    pid_shared = pid
+    if pid_shared < total_x:
+        return 0, pid_shared % nb0_x, pid_shared // nb0_x
+    pid_shared -= total_x
+    return 1, pid_shared % nb0_y, pid_shared // nb0_y
+
+
+def test_golden_helion_multi_loop(golden):
+    grids = [S.grid_for(64, 32, 32, 16), S.grid_for(32, 48, 32, 16)]
+    rows = []
+    for order, mode in ((0, S.BLOCKED), (1, S.INTERLEAVED)):
+        for p, v in enumerate(S.multi_space_schedule(mode, grids, 3)):
+            rows += [(order, p, i, t, s, m, n) for (i, t, s, m, n) in v]
+    assert rows == golden("helion_multi_loop_64x32_32x48.txt")
+
+
+@pytest.mark.parametrize("P", [1, 2, 5, 9])
+def test_multi_loop_matches_helion_branch(P):
+    grids = [S.Grid(3, 4, 1), S.Grid(5, 2, 1)]
+    for mode in (S.BLOCKED, S.INTERLEAVED):
+        for v in S.multi_space_schedule(mode, grids, P):
+            for (_, t, s, m, n) in v:
+                assert (s, m, n) == helion_multi_loop(12, 3, 5, t)
+        ids = sorted(t for v in S.multi_space_schedule(mode, grids, P) for (_, t, _, _, _) in v)
+        assert ids == list(range(22))
