@@ -478,6 +478,17 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
                        "algorithmic_bytes": ADD_BYTES}
     add["workload"] = "fp32 8192x8192 x,y ~ N(0,1) seed 1, out = x + y"
     out["add"] = add
+    # fused multi-space loop (helion multi-loop): result1 = 2 x, result2 = 3 y in one launch
+    r1, r2 = torch.empty_like(tx), torch.empty_like(ty)
+    ml = {}
+    for mode, mname in ((pgt.BLOCKED, "blocked"), (pgt.INTERLEAVED, "interleaved")):
+        fn = lambda: ctx.multi_loop([(tx, r1, 2.0), (ty, r2, 3.0)], sched_mode=mode)  # noqa: E731
+        _, per = time_launches(torch, fn, 30, 3)
+        ms = float(np.median(per))
+        ml[mname] = {"gbs": 2 * 8.0 * ADD_ROWS * ADD_COLS / (ms * 1e-3) / 1e9, "ms": ms}
+    ml["workload"] = "two fp32 8192x8192 spaces in one launch, wide 8x1024 tile; 8 bytes per element"
+    out["multi_loop"] = ml
+    del r1, r2
     del tx, ty, to
     # MXFP8 block-scaled GEMM 8192^3 (E4M3 payload from N(0,1), E8M0 exponents in [-4, 4], seed 4)
     qa, sa, qb, sb = synthetic.gemm_mxfp8_inputs(M, N, K, seed=4)

@@ -246,6 +246,30 @@ int pgt_add(pgt_ctx* ctx, const float* x, const float* y, float* out, int64_t ro
 int pgt_add_workers(const pgt_ctx* ctx, int64_t rows, int64_t cols, int tile_r, int tile_c,
                     int num_workers);
 
+/* ----------------------------------------------------- fused multi-space loop */
+/* One elementwise tile space: out = scale * x over a rows x cols fp32 matrix (row strides
+ * ldx, ldo in elements; 0 = cols).  out may alias x exactly. */
+typedef struct pgt_scale_space {
+    const float* x; /* DEVICE */
+    float* out;     /* DEVICE */
+    int64_t rows, cols, ldx, ldo;
+    float scale;
+    int32_t reserved;
+} pgt_scale_space;
+
+#define PGT_MAX_SPACES 8
+
+/* Several independent tile spaces fused into ONE persistent launch ([PK] the two multi-loop
+ * listings, which compute result1 = 2 * x and result2 = 3 * y): the spaces' tile ids are
+ * laid end to end, P workers walk them in sched_mode PGT_BLOCKED or PGT_INTERLEAVED order,
+ * and each id is decoded inside its own space with tile rows fastest.  Tiles are
+ * tile_r x tile_c (both 0 = the wide 8 x 1024 tile; limits as in pgt_add).  n_spaces in
+ * [1, PGT_MAX_SPACES]; num_workers 0 = every CTA that fits, capped at the tile count.
+ * Traced launches record tile id, m, n, and (space << 24 | SM id) per visit.  Each output
+ * is one IEEE fp32 multiply per element, whatever the order. */
+int pgt_multi_loop(pgt_ctx* ctx, const pgt_scale_space* spaces, int n_spaces, int sched_mode,
+                   int tile_r, int tile_c, int num_workers, const pgt_trace* trace, void* stream);
+
 /* ----------------------------------------------------------- schedule log */
 /* Run only the device tile scheduler (the same code the GEMM kernels run) over an
  * m_blocks x n_blocks grid of CTA tiles with `cluster_size` CTAs per worker, and record

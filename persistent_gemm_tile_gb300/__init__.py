@@ -33,8 +33,9 @@ VISIT_FIELDS = 4
 EXPORTS = (
     "pgt_preamble", "pgt_destroy", "pgt_num_sms", "pgt_max_groups", "pgt_last_error", "pgt_strerror",
     "pgt_gemm_workspace_bytes", "pgt_gemm_plan", "pgt_gemm_ex", "pgt_gemm", "pgt_gemm_host",
-    "pgt_add", "pgt_add_workers", "pgt_schedule_log", "pgt_gemm_noalloc",
+    "pgt_add", "pgt_add_workers", "pgt_schedule_log", "pgt_gemm_noalloc", "pgt_multi_loop",
 )
+MAX_SPACES = 8
 NOALLOC_MAX_GROUPS = 16
 
 
@@ -59,6 +60,12 @@ class PlanInfo(ctypes.Structure):
 class Trace(ctypes.Structure):
     _fields_ = [("visits", ctypes.c_void_p), ("max_visits", ctypes.c_int64),
                 ("counts", ctypes.c_void_p), ("times_ns", ctypes.c_void_p)]
+
+
+class ScaleSpace(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("out", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("ldx", ctypes.c_int64), ("ldo", ctypes.c_int64), ("scale", ctypes.c_float),
+                ("reserved", ctypes.c_int32)]
 
 
 class PgtError(RuntimeError):
@@ -95,6 +102,7 @@ def lib() -> ctypes.CDLL:
         L.pgt_add_workers.argtypes = [P, I64, I64, I, I, I]
         L.pgt_schedule_log.argtypes = [P, I64, I64, I, I, I, I, I, P, P]
         L.pgt_gemm_noalloc.argtypes = [P, P, P, I64, I64, I64, I, I, I, P, P]
+        L.pgt_multi_loop.argtypes = [P, P, I, I, I, I, I, P, P]
         _lib = L
     return _lib
 
@@ -227,6 +235,19 @@ class Context:
         _check(lib().pgt_add(self.handle, _ptr(x), _ptr(y), _ptr(out), rows, cols, ldx, ldy, ldo, sched_mode,
                              tile_r, tile_c, num_workers, ctypes.byref(trace) if trace else None,
                              _stream(stream)), "pgt_add")
+
+    def multi_loop(self, spaces, sched_mode=BLOCKED, tile_r=0, tile_c=0, num_workers=0,
+                   trace: Trace | None = None, stream=None) -> None:
+        """pgt_multi_loop over [(x, out, scale), ...] 2-D fp32 tensors: out = scale * x."""
+        if isinstance(sched_mode, str):
+            sched_mode = SCHED[sched_mode]
+        arr = (ScaleSpace * len(spaces))()
+        for i, (x, out, scale) in enumerate(spaces):
+            arr[i] = ScaleSpace(_ptr(x), _ptr(out), x.shape[0], x.shape[1], x.stride(0), out.stride(0),
+                                float(scale), 0)
+        _check(lib().pgt_multi_loop(self.handle, ctypes.cast(arr, ctypes.c_void_p), len(spaces), sched_mode, tile_r,
+                                    tile_c, num_workers, ctypes.byref(trace) if trace else None, _stream(stream)),
+               "pgt_multi_loop")
 
     def add_workers(self, rows, cols, tile_r=0, tile_c=0, num_workers=0) -> int:
         return _check(lib().pgt_add_workers(self.handle, rows, cols, tile_r, tile_c, num_workers),

@@ -53,7 +53,7 @@ def test_binding_constants_match_header():
         "PGT_CFG_1CTA_128x256": pgt.CFG_1CTA_128x256, "PGT_CFG_2CTA_256x128": pgt.CFG_2CTA_256x128,
         "PGT_CFG_2CTA_256x256": pgt.CFG_2CTA_256x256, "PGT_FLAG_HOST_RESET": pgt.FLAG_HOST_RESET,
         "PGT_VISIT_FIELDS": pgt.VISIT_FIELDS, "PGT_NOALLOC_MAX_GROUPS": pgt.NOALLOC_MAX_GROUPS,
-        "PGT_EPI_ALPHA": pgt.EPI_ALPHA, "PGT_EPI_BIAS": pgt.EPI_BIAS,
+        "PGT_EPI_ALPHA": pgt.EPI_ALPHA, "PGT_EPI_BIAS": pgt.EPI_BIAS, "PGT_MAX_SPACES": pgt.MAX_SPACES,
     }
     for k, v in pairs.items():
         assert d[k] == v, k
@@ -63,6 +63,7 @@ def test_struct_sizes_match_c_layout():
     assert ctypes.sizeof(pgt.GemmDesc) == 6 * 8 + 10 * 4 + 8
     assert ctypes.sizeof(pgt.PlanInfo) == 14 * 4
     assert ctypes.sizeof(pgt.Trace) == 32
+    assert ctypes.sizeof(pgt.ScaleSpace) == 2 * 8 + 4 * 8 + 8
 
 
 def test_strerror_names_every_status(lib):
