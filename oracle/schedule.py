@@ -153,9 +153,18 @@ class WsState:
         self.cursor = [0] * P  # groups already found exhausted, counted from home
         self.done = [False] * P
 
-    def fetch(self, c: int) -> int:
-        """One fetch by worker c; returns a tile id or -1 once every group is exhausted."""
+    def fetch(self, c: int, released=frozenset()) -> int:
+        """One fetch by worker c; returns a tile id or -1 once every group is exhausted.
+
+        Cooperative release (tritonBLAS "Work Stealing Scheduler Kernel", the commits "one
+        live flag per XCD" and "Request CU release"; the mechanism is not on the page).
+        Reading: before each fetch a worker reads its home group's flag and, if the group is
+        in ``released``, stops taking tiles; group 0 is never released, so its workers
+        always finish the remaining tiles by stealing."""
         home = c % self.groups
+        if home != 0 and home in released:
+            self.done[c] = True
+            return -1
         while self.cursor[c] < self.groups:
             g = (home + self.cursor[c]) % self.groups
             ticket = self.counter[g]
@@ -168,14 +177,18 @@ class WsState:
         return -1
 
 
-def ws_simulate(T: int, P: int, groups: int, pick) -> list[list[int]]:
-    """Run the protocol with workers fetching in the order chosen by ``pick(live) -> c``."""
+def ws_simulate(T: int, P: int, groups: int, pick, release_at=None) -> list[list[int]]:
+    """Run the protocol with workers fetching in the order chosen by ``pick(live) -> c``.
+    ``release_at(step) -> set of released groups`` models flags raised while it runs."""
     st = WsState(T, P, groups)
     visits: list[list[int]] = [[] for _ in range(P)]
     live = list(range(P))
+    step = 0
     while live:
         c = pick(live)
-        t = st.fetch(c)
+        released = release_at(step) if release_at else frozenset()
+        step += 1
+        t = st.fetch(c, released)
         if t < 0:
             live.remove(c)
         else:

@@ -267,3 +267,24 @@ def test_multi_loop_matches_helion_branch(P):
                 assert (s, m, n) == helion_multi_loop(12, 3, 5, t)
         ids = sorted(t for v in S.multi_space_schedule(mode, grids, P) for (_, t, _, _, _) in v)
         assert ids == list(range(22))
+
+
+# ------------------------------------------------------------------ cooperative release
+@pytest.mark.parametrize("seed", range(12))
+def test_ws_release_still_covers_every_tile(seed):
+    rnd = random.Random(100 + seed)
+    T, P, G = rnd.randint(1, 300), rnd.randint(1, 24), rnd.choice([2, 3, 8])
+    rel = frozenset(rnd.sample(range(G), rnd.randint(1, G)))
+    switch = rnd.randint(0, T)
+    visits = S.ws_simulate(T, P, G, lambda live: rnd.choice(live),
+                           release_at=lambda step: rel if step >= switch else frozenset())
+    S.check_ws_trace(visits, T, G)
+
+
+def test_ws_release_from_the_start_leaves_all_to_group_zero():
+    T, P, G = 100, 16, 4
+    rnd = random.Random(5)
+    visits = S.ws_simulate(T, P, G, lambda live: rnd.choice(live), release_at=lambda step: frozenset({0, 1, 2, 3}))
+    S.check_ws_trace(visits, T, G)
+    assert all(not v for c, v in enumerate(visits) if c % G != 0)
+    assert sum(len(v) for c, v in enumerate(visits) if c % G == 0) == T
