@@ -167,6 +167,18 @@ int pgt_preamble(int device, int max_groups, int flags, pgt_ctx** out);
 /* Free a context (synchronises its device first).  NULL is accepted. */
 int pgt_destroy(pgt_ctx* ctx);
 
+/* Cooperative release of work-stealing workers ([WS] commits "Changing to one live flag per
+ * XCD" and "Request CU release from the scheduler kernel", which spin on host memory; this
+ * is a bounded rework).  Copies n flags (host int32, nonzero = release) into the context's
+ * per-group device flags with cudaMemcpyAsync on `stream` — which may differ from the
+ * stream of a running GEMM, so a release can land mid-launch.  Before every tile fetch a
+ * WORK_STEALING worker reads its home group's flag once (no spinning) and, if it is raised,
+ * takes no further tiles; the other workers steal what is left, so the output is complete
+ * and identical.  Group 0 is never released (its workers always finish the GEMM).  Flags
+ * stay raised until cleared by another call; static modes ignore them.  n in
+ * [1, max_groups]; pinned host memory keeps the copy asynchronous. */
+int pgt_set_release(pgt_ctx* ctx, const int32_t* h_flags, int n, void* stream);
+
 /* SM count of the context's device, or a negative status for a NULL context. */
 int pgt_num_sms(const pgt_ctx* ctx);
 

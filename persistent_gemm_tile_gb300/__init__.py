@@ -33,7 +33,7 @@ VISIT_FIELDS = 4
 EXPORTS = (
     "pgt_preamble", "pgt_destroy", "pgt_num_sms", "pgt_max_groups", "pgt_last_error", "pgt_strerror",
     "pgt_gemm_workspace_bytes", "pgt_gemm_plan", "pgt_gemm_ex", "pgt_gemm", "pgt_gemm_host",
-    "pgt_add", "pgt_add_workers", "pgt_schedule_log", "pgt_gemm_noalloc", "pgt_multi_loop",
+    "pgt_add", "pgt_add_workers", "pgt_schedule_log", "pgt_gemm_noalloc", "pgt_multi_loop", "pgt_set_release",
 )
 MAX_SPACES = 8
 NOALLOC_MAX_GROUPS = 16
@@ -103,6 +103,7 @@ def lib() -> ctypes.CDLL:
         L.pgt_schedule_log.argtypes = [P, I64, I64, I, I, I, I, I, P, P]
         L.pgt_gemm_noalloc.argtypes = [P, P, P, I64, I64, I64, I, I, I, P, P]
         L.pgt_multi_loop.argtypes = [P, P, I, I, I, I, I, P, P]
+        L.pgt_set_release.argtypes = [P, P, I, P]
         _lib = L
     return _lib
 
@@ -176,6 +177,13 @@ class Context:
             self.close()
         except Exception:
             pass
+
+    def set_release(self, flags, stream=None) -> None:
+        """pgt_set_release: raise (nonzero) or clear the per-group release flags."""
+        import numpy as np
+        arr = np.ascontiguousarray(flags, dtype=np.int32)
+        self._release_host = arr  # the copy is asynchronous: keep the host buffer alive
+        _check(lib().pgt_set_release(self.handle, arr.ctypes.data, arr.size, _stream(stream)), "pgt_set_release")
 
     @property
     def num_sms(self) -> int:

@@ -194,6 +194,7 @@ int add_launch(pgt_ctx* ctx, const float* x, const float* y, float* out, int64_t
     p.sp.workers = workers;
     p.sp.counters = nullptr;
     p.sp.done = nullptr;
+    p.sp.release = nullptr;
     p.tr_visits = trace ? trace->visits : nullptr;
     p.tr_max = trace ? trace->max_visits : 0;
     p.tr_counts = trace ? trace->counts : nullptr;

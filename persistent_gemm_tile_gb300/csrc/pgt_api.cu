@@ -67,6 +67,7 @@ int schedule_log_launch(pgt_ctx* ctx, int64_t m_blocks, int64_t n_blocks, int cl
     sp.workers = num_workers;
     sp.counters = ctx->d_counters;
     sp.done = ctx->d_done;
+    sp.release = ctx->d_release;
     if (sched_mode == PGT_WORK_STEALING && (ctx->flags & PGT_FLAG_HOST_RESET)) {
         if (cudaMemsetAsync(ctx->d_counters, 0, sizeof(int) * kCounterStride * (ctx->max_groups + 1), stream) !=
             cudaSuccess)
@@ -94,8 +95,9 @@ int pgt_preamble(int device, int max_groups, int flags, pgt_ctx** out) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || sms < 1)
         return PGT_ERR_CUDA;
-    // counters: max_groups lines, then the done counter's line, then the error word's line
-    const size_t bytes = sizeof(int) * kCounterStride * (max_groups + 2);
+    // counters: max_groups lines, then the done counter's line, the error word's line and
+    // two lines of release flags
+    const size_t bytes = sizeof(int) * kCounterStride * (max_groups + 4);
     void* blk = nullptr;
     if (cudaMalloc(&blk, bytes) != cudaSuccess) return PGT_ERR_CUDA;
     if (cudaMemset(blk, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
@@ -115,6 +117,7 @@ int pgt_preamble(int device, int max_groups, int flags, pgt_ctx** out) {
     c->d_counters = static_cast<int*>(blk);
     c->d_done = c->d_counters + kCounterStride * max_groups;
     c->d_err = c->d_done + kCounterStride;
+    c->d_release = c->d_err + kCounterStride;
     *out = c;
     return PGT_OK;
 }
@@ -130,6 +133,13 @@ int pgt_destroy(pgt_ctx* ctx) {
     if (prev >= 0) cudaSetDevice(prev);
     free(ctx);
     return rc;
+}
+
+int pgt_set_release(pgt_ctx* ctx, const int32_t* h_flags, int n, void* stream) {
+    if (ctx == nullptr || h_flags == nullptr || n < 1 || n > ctx->max_groups) return PGT_ERR_ARG;
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return PGT_ERR_CUDA;
+    return cuda_status(cudaMemcpyAsync(ctx->d_release, h_flags, sizeof(int32_t) * n, cudaMemcpyHostToDevice,
+                                       static_cast<cudaStream_t>(stream)));
 }
 
 int pgt_num_sms(const pgt_ctx* ctx) { return ctx ? ctx->num_sms : PGT_ERR_ARG; }

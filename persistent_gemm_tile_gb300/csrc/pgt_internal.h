@@ -15,6 +15,7 @@ struct pgt_ctx {
     int* d_counters;  // max_groups counters, kCounterStride ints apart, zero between launches
     int* d_done;      // work-stealing done counter (own 128-byte line)
     int* d_err;       // device error word: code, role, block, site
+    int* d_release;   // work-stealing release flags, one int per group (two 128-byte lines)
     void* d_block;    // the single allocation holding the three above
 };
 

@@ -181,6 +181,7 @@ extern "C" int pgt_multi_loop(pgt_ctx* ctx, const pgt_scale_space* spaces, int n
     p.sched.workers = workers;
     p.sched.counters = nullptr;
     p.sched.done = nullptr;
+    p.sched.release = nullptr;
     p.tr_visits = trace ? trace->visits : nullptr;
     p.tr_max = trace ? trace->max_visits : 0;
     p.tr_counts = trace ? trace->counts : nullptr;

@@ -74,6 +74,7 @@ extern "C" int pgt_gemm_noalloc(const void* A, const void* B, void* C, int64_t M
     c.d_counters = ds.scratch;
     c.d_done = ds.scratch + pgt::kCounterStride * PGT_NOALLOC_MAX_GROUPS;
     c.d_err = d_err != nullptr ? d_err : c.d_done + pgt::kCounterStride;
+    c.d_release = nullptr;
     c.d_block = nullptr;
 
     pgt_gemm_desc in = {};

@@ -30,6 +30,7 @@ struct SchedParams {
     int workers;    // P
     int* counters;  // ws_groups * kCounterStride ints, zero at launch
     int* done;      // workers that have finished fetching
+    const int* release;  // work stealing: per-group release flags (may be null)
 };
 
 // Linear decode: tile rows vary fastest (helion pid_0 = vpid % num_blocks_0).
@@ -115,6 +116,11 @@ struct Scheduler {
     // Next tile id, or -1 when this worker is done.
     __device__ __forceinline__ int fetch() {
         if (p.mode == kWorkStealing) {
+            // cooperative release: a raised flag of the home group (never group 0, whose
+            // workers finish whatever is left) stops this worker before its next tile
+            if (p.release != nullptr && home != 0 &&
+                *reinterpret_cast<const volatile int*>(p.release + home) != 0)
+                return -1;
             while (cursor < p.ws_groups) {
                 int g = home + cursor;
                 if (g >= p.ws_groups) g -= p.ws_groups;
