@@ -41,13 +41,14 @@ from __future__ import annotations
 
 from dataclasses import dataclass
 
-BLOCKED, INTERLEAVED, SWIZZLED, WORK_STEALING, BLOCKED_GROUPED_M = 0, 1, 2, 3, 4
+BLOCKED, INTERLEAVED, SWIZZLED, WORK_STEALING, BLOCKED_GROUPED_M, LAUNCH_CONTROL = 0, 1, 2, 3, 4, 5
 MODE_NAMES = {
     BLOCKED: "blocked",
     INTERLEAVED: "interleaved",
     SWIZZLED: "swizzled",
     WORK_STEALING: "work_stealing",
     BLOCKED_GROUPED_M: "blocked_grouped_m",
+    LAUNCH_CONTROL: "launch_control",
 }
 
 
@@ -104,7 +105,7 @@ def decode(mode: int, t: int, grid: Grid, G: int) -> tuple[int, int]:
         return decode_linear(t, mc)
     if mode == BLOCKED_GROUPED_M:
         return decode_grouped_m(t, max(G, 1), mc, nb)
-    if mode in (SWIZZLED, WORK_STEALING):
+    if mode in (SWIZZLED, WORK_STEALING, LAUNCH_CONTROL):
         if G <= 1:
             return decode_linear(t, mc)
         return decode_swizzled(t, G, mc, nb)
@@ -241,3 +242,22 @@ def multi_space_schedule(mode: int, grids: list[Grid], P: int) -> list[list[tupl
             visits.append((i, t, s, m, n))
         out.append(visits)
     return out
+
+
+# ------------------------------------------------------------- hardware launch control
+def check_launch_control_trace(visits: list[list[int]], T: int) -> None:
+    """Validate a launch-control visit log: one list per launched worker w = 0..T-1 (one per
+    tile), tile ids in visit order.  Dynamic scheduling through the hardware (an idiomatic
+    Blackwell counterpart of the atomic counters, not on the pages): a worker that ran
+    starts with its own tile w and then takes the tiles of workers it cancelled before they
+    started; a cancelled worker visits nothing.  Raises AssertionError unless every tile is
+    visited exactly once, every non-empty list starts with its own id, and every tile other
+    than a list's first belongs to a worker whose own list is empty."""
+    assert len(visits) == T, "one list per tile-worker expected"
+    flat = sorted(t for v in visits for t in v)
+    assert flat == list(range(T)), "launch-control visits are not a permutation of the tiles"
+    for w, v in enumerate(visits):
+        if v:
+            assert v[0] == w, f"worker {w} did not start with its own tile"
+            for t in v[1:]:
+                assert not visits[t], f"tile {t} was taken from a worker that also ran"

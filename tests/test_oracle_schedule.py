@@ -288,3 +288,33 @@ def test_ws_release_from_the_start_leaves_all_to_group_zero():
     S.check_ws_trace(visits, T, G)
     assert all(not v for c, v in enumerate(visits) if c % G != 0)
     assert sum(len(v) for c, v in enumerate(visits) if c % G == 0) == T
+
+
+# ------------------------------------------------------------------ launch control
+def _clc_trace():
+    # workers 0 and 3 ran; 0 took the tiles of workers 1, 2, 5; 3 took 4
+    return [[0, 1, 2, 5], [], [], [3, 4], [], []]
+
+
+def test_launch_control_checker_accepts_valid_and_decodes_like_swizzled():
+    S.check_launch_control_trace(_clc_trace(), 6)
+    grid = S.Grid(5, 7, 2)
+    for t in range(grid.tiles):
+        assert S.decode(S.LAUNCH_CONTROL, t, grid, 4) == S.decode(S.SWIZZLED, t, grid, 4)
+
+
+@pytest.mark.parametrize("plant", ["dup", "drop", "first", "ran_twice"])
+def test_launch_control_checker_rejects_planted_mistakes(plant):
+    v = [list(x) for x in _clc_trace()]
+    if plant == "dup":
+        v[3].append(1)
+    elif plant == "drop":
+        v[0].pop()
+    elif plant == "first":
+        v[3] = [4, 3]
+    elif plant == "ran_twice":  # worker 2 also ran its own tile, yet 0 claims to have taken it
+        v[2] = [2]
+        v[0].remove(5)
+        v[3].append(5)
+    with pytest.raises(AssertionError):
+        S.check_launch_control_trace(v, 6)
