@@ -399,7 +399,8 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
     # the same mix of power and clock states; median per-launch time
     per_mode = {}
     names = {pgt.BLOCKED: "blocked", pgt.INTERLEAVED: "interleaved", pgt.SWIZZLED: "swizzled",
-             pgt.WORK_STEALING: "work_stealing", pgt.BLOCKED_GROUPED_M: "blocked_grouped_m"}
+             pgt.WORK_STEALING: "work_stealing", pgt.BLOCKED_GROUPED_M: "blocked_grouped_m",
+             pgt.LAUNCH_CONTROL: "launch_control"}
     samples = {name: [] for name in names.values()}
     descs = {mode: desc_for(mode) for mode in names}
     for _ in range(6):
@@ -538,7 +539,8 @@ def ragged_set(torch, pgt, ctx, device):
     shapes = [(4864, 4096, 2048), (128, 16384, 16384), (3000, 5000, 1024)]
     res = {}
     names = {pgt.BLOCKED: "blocked", pgt.INTERLEAVED: "interleaved", pgt.SWIZZLED: "swizzled",
-             pgt.WORK_STEALING: "work_stealing", pgt.BLOCKED_GROUPED_M: "blocked_grouped_m"}
+             pgt.WORK_STEALING: "work_stealing", pgt.BLOCKED_GROUPED_M: "blocked_grouped_m",
+             pgt.LAUNCH_CONTROL: "launch_control"}
     for (m, n, k), (a, b) in zip(shapes, synthetic.gemm_bf16_sequence(shapes, seed=3, dist="uniform")):
         ta = torch.from_numpy(a.view(np.int16)).to(device)
         tb_ = torch.from_numpy(b.view(np.int16)).to(device)

@@ -80,6 +80,13 @@ extern "C" {
 #define PGT_SWIZZLED 2
 #define PGT_WORK_STEALING 3
 #define PGT_BLOCKED_GROUPED_M 4
+/*   LAUNCH_CONTROL:    dynamic scheduling done by the hardware (Blackwell cluster launch
+ *                      control; not on the pages, the GB300 counterpart of the atomic
+ *                      counters): one worker is launched per tile; a running worker takes
+ *                      its own tile, then asks the hardware to cancel a worker that has not
+ *                      started yet and takes that worker's tile, until none is left.  Tiles
+ *                      decoded like SWIZZLED.  P = T (num_workers must be 0 or T). */
+#define PGT_LAUNCH_CONTROL 5
 
 /* GEMM kernel configurations (output tile per worker, CTAs per worker).
  *   1CTA_128x128 / 1CTA_128x256: one CTA, tcgen05 cta_group::1, M=128 MMAs.

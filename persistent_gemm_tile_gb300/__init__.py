@@ -21,9 +21,9 @@ ERR_ARG, ERR_ALIGN, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_GROUPS, ERR_WORK
     -1, -2, -3, -4, -5, -6, -7, -8)
 BF16, MXFP8 = 0, 1
 B_KN, B_NK = 0, 1
-BLOCKED, INTERLEAVED, SWIZZLED, WORK_STEALING, BLOCKED_GROUPED_M = 0, 1, 2, 3, 4
+BLOCKED, INTERLEAVED, SWIZZLED, WORK_STEALING, BLOCKED_GROUPED_M, LAUNCH_CONTROL = 0, 1, 2, 3, 4, 5
 SCHED = {"blocked": BLOCKED, "interleaved": INTERLEAVED, "swizzled": SWIZZLED,
-         "work_stealing": WORK_STEALING, "blocked_grouped_m": BLOCKED_GROUPED_M}
+         "work_stealing": WORK_STEALING, "blocked_grouped_m": BLOCKED_GROUPED_M, "launch_control": LAUNCH_CONTROL}
 CFG_AUTO, CFG_1CTA_128x128, CFG_1CTA_128x256, CFG_2CTA_256x128, CFG_2CTA_256x256 = 0, 1, 2, 3, 4
 FLAG_HOST_RESET = 1
 EPI_ALPHA, EPI_BIAS = 1, 2

@@ -10,16 +10,44 @@
 namespace pgt {
 
 // One thread per worker runs the device scheduler and records its visits (no GEMM work).
+// Launch control: one block per tile; a running block takes its own tile, then the tiles
+// of blocks it cancels before they start.
 __global__ void schedule_log_kernel(const SchedParams sp, int32_t* visits, int64_t max_visits, int32_t* counts,
-                                    int64_t* times) {
+                                    int64_t* times, int* err) {
+    __shared__ __align__(16) uint8_t clc_resp[16];
+    __shared__ __align__(8) uint64_t clc_bar_word;
     if (threadIdx.x != 0) return;
     const int w = blockIdx.x;
     if (times != nullptr) times[2 * w] = (int64_t)globaltimer();
     Scheduler sch;
     sch.init(sp, w);
+    const bool clc = sp.mode == kLaunchControl;
+    const uint32_t clc_bar = smem_u32(&clc_bar_word), resp = smem_u32(clc_resp);
+    if (clc) {
+        mbar_init(clc_bar, 1);
+        fence_mbar_init();
+    }
+    volatile int abort_local = 0;
+    uint32_t phase = 0;
+    int next = w;
     int n = 0;
     for (;;) {
-        const int t = sch.fetch();
+        int t;
+        if (clc) {
+            t = next;
+            if (t < 0) break;
+            mbar_arrive_expect_tx(clc_bar, 16);
+            clc_try_cancel(resp, clc_bar);
+            next = -1;
+            volatile int no_abort = 0;
+            if (mbar_wait(clc_bar, phase & 1u, &no_abort, err, kRoleScheduler, 11) && !abort_local) {
+                const int x = clc_query(resp);
+                next = (x < 0 || x >= sp.tiles) ? -1 : x;
+            }
+            ++phase;
+        } else {
+            t = sch.fetch();
+        }
         if (t < 0) break;
         int m, nn;
         decode_tile(sp, t, m, nn);
@@ -44,13 +72,14 @@ int schedule_log_launch(pgt_ctx* ctx, int64_t m_blocks, int64_t n_blocks, int cl
         trace->max_visits < 1)
         return PGT_ERR_ARG;
     if (m_blocks < 1 || n_blocks < 1 || (cluster_size != 1 && cluster_size != 2)) return PGT_ERR_ARG;
-    if (sched_mode < PGT_BLOCKED || sched_mode > PGT_BLOCKED_GROUPED_M || group_size < 1 || num_workers < 1)
+    if (sched_mode < PGT_BLOCKED || sched_mode > PGT_LAUNCH_CONTROL || group_size < 1 || num_workers < 1)
         return PGT_ERR_ARG;
     if (ws_groups < 1 || ws_groups > ctx->max_groups) return PGT_ERR_GROUPS;
     const int64_t m_tiles = (m_blocks + cluster_size - 1) / cluster_size;
     const int64_t tiles = m_tiles * n_blocks;
     if (m_blocks >= ((int64_t)1 << 31) || n_blocks >= ((int64_t)1 << 31) || tiles >= ((int64_t)1 << 31))
         return PGT_ERR_ARG;
+    if (sched_mode == PGT_LAUNCH_CONTROL && num_workers != tiles) return PGT_ERR_ARG;  // one per tile
     SchedParams sp;
     sp.tiles = (int)tiles;
     sp.m_tiles = (int)m_tiles;
@@ -74,7 +103,7 @@ int schedule_log_launch(pgt_ctx* ctx, int64_t m_blocks, int64_t n_blocks, int cl
             return PGT_ERR_CUDA;
     }
     schedule_log_kernel<<<num_workers, 32, 0, stream>>>(sp, trace->visits, trace->max_visits, trace->counts,
-                                                       trace->times_ns);
+                                                       trace->times_ns, ctx->d_err);
     return cuda_status(cudaGetLastError());
 }
 

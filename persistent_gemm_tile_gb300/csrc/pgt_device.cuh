@@ -138,6 +138,32 @@ __device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr, int a, int b
                  : "memory");
 }
 
+// ------------------------------------------------------- cluster launch control
+// Ask the hardware to cancel the launch of a cluster that has not started yet; the 16-byte
+// answer lands in shared memory and completes 16 transaction bytes on `bar`.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp_smem, uint32_t bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+            resp_smem),
+        "r"(bar)
+        : "memory");
+}
+
+// Decode an answer: the x index of the first CTA of the cancelled cluster, or -1 when
+// nothing was cancelled (no cluster left to take; no further request may follow).
+__device__ __forceinline__ int clc_query(uint32_t resp_smem) {
+    int x = -1;
+    asm volatile(
+        "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+        "ld.shared.b128 r, [%1];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, r;\n\t}\n"
+        : "+r"(x)
+        : "r"(resp_smem)
+        : "memory");
+    return x;
+}
+
 // ------------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int32_t x, int32_t y) {

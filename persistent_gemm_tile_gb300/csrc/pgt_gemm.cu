@@ -81,11 +81,12 @@ struct Layout {
     static constexpr int EPI_BUFS = (STAGES * STAGE_BYTES + kEpiWarps * 2 * kEpiBufBytes + 2048 <= kMaxSmem) ? 2 : 1;
     static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
     static constexpr int BAR_OFF = EPI_OFF + kEpiWarps * EPI_BUFS * kEpiBufBytes;
-    // barriers: full[S], empty[S], tfull[2], tempty[2], sfull[Q], sempty[Q], mma_done
-    static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * kTileRing + 1;
+    // barriers: full[S], empty[S], tfull[2], tempty[2], sfull[Q], sempty[Q], mma_done, clc
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * kTileRing + 2;
     static constexpr int RING_OFF = BAR_OFF + (NUM_BARS * 8 + 15) / 16 * 16;  // int4 entries
     static constexpr int MISC_OFF = RING_OFF + kTileRing * 16;                // tmem slot, abort flag
-    static constexpr int BYTES = MISC_OFF + 16;
+    static constexpr int CLC_OFF = MISC_OFF + 16;                             // launch-control answer
+    static constexpr int BYTES = CLC_OFF + 16;
     static constexpr int SMEM = BYTES + 1024;  // alignment slack
     static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0 && (A_BYTES + B_BYTES) % 1024 == 0,
                   "stages must keep 1024-byte swizzle alignment");
@@ -150,6 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto sfull = [&](int q) { return bar0 + 8u * (2 * STAGES + 4 + q); };
     auto sempty = [&](int q) { return bar0 + 8u * (2 * STAGES + 4 + kTileRing + q); };
     const uint32_t mma_done = bar0 + 8u * (2 * STAGES + 4 + 2 * kTileRing);
+    const uint32_t clc_bar = mma_done + 8u;
+    const uint32_t clc_resp = base + L::CLC_OFF;
     int4* ring = reinterpret_cast<int4*>(gbase + L::RING_OFF);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + L::MISC_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + L::MISC_OFF + 4);
@@ -170,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(sempty(q), kPair ? 2 + 2 * kEpiWarps : 1 + kEpiWarps);
         }
         mbar_init(mma_done, 1);
+        mbar_init(clc_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -198,6 +202,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             Scheduler sch;
             if (leader) sch.init(gp.sp, worker);
+            const bool clc = gp.sp.mode == kLaunchControl;
+            bool clc_first = true, clc_pending = false;
+            uint32_t clc_phase = 0;
+            // launch control: the worker's own tile first, then tiles of clusters it cancels
+            // before they start; one request in flight, issued as soon as a tile is taken
+            auto clc_fetch = [&]() -> int {
+                int t = -1;
+                if (clc_first) {
+                    clc_first = false;
+                    t = worker;
+                } else if (clc_pending) {
+                    clc_pending = false;
+                    if (mbar_wait(clc_bar, clc_phase & 1u, abort_flag, gp.err, kRoleScheduler, 9)) {
+                        const int x = clc_query(clc_resp);
+                        t = (x < 0 || x / CS >= gp.sp.tiles) ? -1 : x / CS;
+                    }
+                    ++clc_phase;
+                }
+                if (t >= 0 && !*abort_flag) {
+                    mbar_arrive_expect_tx(clc_bar, 16);
+                    clc_try_cancel(clc_resp, clc_bar);
+                    clc_pending = true;
+                }
+                return t;
+            };
             uint32_t it = 0, qc = 0;
             int nvis = 0;
             bool ok = true;
@@ -206,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int q = qc % kTileRing;
                 const uint32_t qpar = (qc / kTileRing) & 1u;
                 if (leader) {
-                    t = *abort_flag ? -1 : sch.fetch();
+                    t = *abort_flag ? -1 : (clc ? clc_fetch() : sch.fetch());
                     if (t >= 0) decode_tile(gp.sp, t, m, n);
                     if (!mbar_wait<kPair>(sempty(q), qpar ^ 1u, abort_flag, gp.err, kRoleProducer, 0)) break;
                     ring[q] = make_int4(t, m, n, 0);
@@ -268,6 +297,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (leader) sch.finish();
+            if (clc_pending) {
+                // never leave with an answer still to land in this CTA's shared memory
+                volatile int no_abort = 0;
+                mbar_wait(clc_bar, clc_phase & 1u, &no_abort, gp.err, kRoleScheduler, 10);
+            }
             if (TRACE && gp.tr_counts != nullptr) gp.tr_counts[blockIdx.x] = nvis;
         }
         __syncwarp();
@@ -677,7 +711,7 @@ int gemm_plan(const pgt_ctx* ctx, const pgt_gemm_desc* in, pgt_gemm_desc* d, pgt
     if (d->M < 1 || d->N < 1 || d->K < 1 || d->M >= lim || d->N >= lim || d->K >= lim) return PGT_ERR_ARG;
     if (d->dtype != PGT_BF16 && d->dtype != PGT_MXFP8) return PGT_ERR_ARG;
     if (d->b_layout != PGT_B_KN && d->b_layout != PGT_B_NK) return PGT_ERR_ARG;
-    if (d->sched_mode < PGT_BLOCKED || d->sched_mode > PGT_BLOCKED_GROUPED_M) return PGT_ERR_ARG;
+    if (d->sched_mode < PGT_BLOCKED || d->sched_mode > PGT_LAUNCH_CONTROL) return PGT_ERR_ARG;
     if (d->group_size < 1) return PGT_ERR_ARG;
     if (d->num_workers < 0) return PGT_ERR_ARG;
     if (d->ws_groups == 0) d->ws_groups = ctx->max_groups < 8 ? ctx->max_groups : 8;
@@ -703,7 +737,11 @@ int gemm_plan(const pgt_ctx* ctx, const pgt_gemm_desc* in, pgt_gemm_desc* d, pgt
     const int64_t tiles = m_tiles * n_blocks;
     if (tiles >= lim) return PGT_ERR_ARG;
     int64_t workers = d->num_workers;
-    if (workers == 0) {
+    if (d->sched_mode == PGT_LAUNCH_CONTROL) {
+        // one worker (CTA or pair) per tile; the hardware cancels the ones not yet started
+        if (workers != 0 && workers != tiles) return PGT_ERR_ARG;
+        workers = tiles;
+    } else if (workers == 0) {
         KernelInfo ki;
         int rc = kernel_info(ctx->device, d->kernel_cfg, d->dtype == PGT_MXFP8, d->b_layout == PGT_B_KN, false, s,
                              &ki);

@@ -14,7 +14,8 @@
 
 namespace pgt {
 
-enum : int { kBlocked = 0, kInterleaved = 1, kSwizzled = 2, kWorkStealing = 3, kBlockedGroupedM = 4 };
+enum : int { kBlocked = 0, kInterleaved = 1, kSwizzled = 2, kWorkStealing = 3, kBlockedGroupedM = 4,
+             kLaunchControl = 5 };
 
 // One counter per 128-byte line so counters of different groups never share a line
 // ("8-way spread contention" in the tritonBLAS PR).

@@ -49,6 +49,7 @@ def test_binding_constants_match_header():
         "PGT_BF16": pgt.BF16, "PGT_MXFP8": pgt.MXFP8, "PGT_B_KN": pgt.B_KN, "PGT_B_NK": pgt.B_NK,
         "PGT_BLOCKED": pgt.BLOCKED, "PGT_INTERLEAVED": pgt.INTERLEAVED, "PGT_SWIZZLED": pgt.SWIZZLED,
         "PGT_WORK_STEALING": pgt.WORK_STEALING, "PGT_BLOCKED_GROUPED_M": pgt.BLOCKED_GROUPED_M,
+        "PGT_LAUNCH_CONTROL": pgt.LAUNCH_CONTROL,
         "PGT_CFG_AUTO": pgt.CFG_AUTO, "PGT_CFG_1CTA_128x128": pgt.CFG_1CTA_128x128,
         "PGT_CFG_1CTA_128x256": pgt.CFG_1CTA_128x256, "PGT_CFG_2CTA_256x128": pgt.CFG_2CTA_256x128,
         "PGT_CFG_2CTA_256x256": pgt.CFG_2CTA_256x256, "PGT_FLAG_HOST_RESET": pgt.FLAG_HOST_RESET,
