@@ -72,6 +72,9 @@ def parse():
     ap.add_argument("--ragged", action="store_true",
                     help="also time the ragged-tail GEMM set per scheduler, with tail idle from traces")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
+    ap.add_argument("--size", type=int, default=8192,
+                    help="M = N = K of the GEMM workloads (8192 is the benchmark; smaller sizes are for "
+                         "quick checks and small profiling cases)")
     return ap.parse_args()
 
 
@@ -205,7 +208,7 @@ def cpu_baseline(budget_s: float, A_bits, B_bits, rows_hint: int | None = None) 
     OG.gemm_rows(A64, B64, True, K, N, np.arange(rows))
     dt = time.perf_counter() - t0
     return {"value": 2.0 * rows * N * K / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"first {rows} rows of C for the 8192^3 bf16 GEMM (fp64 C loops, OpenMP over rows), "
+            "sample": f"first {rows} rows of C for the {M}^3 bf16 GEMM (fp64 C loops, OpenMP over rows), "
                       f"{dt:.1f} s; operand decode not timed"}
 
 
@@ -242,7 +245,7 @@ def run_reference(args, world, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "sample_rows_per_step": rows},
         "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{rows} rows of C per step of the 8192^3 bf16 GEMM, fp64 oracle"},
+                         "sample": f"{rows} rows of C per step of the {M}^3 bf16 GEMM, fp64 oracle"},
         "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -380,7 +383,7 @@ def run_mx_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peaks
            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": "e4m3+e8m0", "data": "synthetic",
-           "config": {"workload": "MXFP8 8192^3 seed 4, swizzled group 16", "kernel_cfg": plan["kernel_cfg"],
+           "config": {"workload": f"MXFP8 {M}^3 seed 4, swizzled group 16", "kernel_cfg": plan["kernel_cfg"],
                       "tile": f"{plan['bm'] * plan['cluster_size']}x{plan['bn']}", "l2": L2_NOTE},
            "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
                         "frac": achieved / fp8_peak, "traffic": None,
@@ -456,7 +459,7 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
         ctx.gemm_ex(d, dA, dB, dC, trace=tb.struct)
         torch.cuda.synchronize()
         tails[name] = tail_idle(tb.times.cpu().numpy())
-    out["tail_idle"] = {"workload": "8192^3 bf16", **tails}
+    out["tail_idle"] = {"workload": f"{M}^3 bf16", **tails}
     # persistent add
     x, y = synthetic.add_inputs(ADD_ROWS, ADD_COLS, seed=1)
     tx, ty = torch.from_numpy(x).to(device), torch.from_numpy(y).to(device)
@@ -512,7 +515,7 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
                       "traffic": profiled_traffic("gemm_mxfp8_2cta_256x256") if best == "2cta_256x256" else None,
                       "kernel": best,
                       "peak_kind": f"2 x measured bf16 burst ({peaks['source']}), nominal fp8/bf16 ratio"}
-    mx["workload"] = "MXFP8 8192^3, E4M3 payload N(0,1), E8M0 per 1x128 K block, exps U{-4..4}, seed 4, " \
+    mx["workload"] = f"MXFP8 {M}^3, E4M3 payload N(0,1), E8M0 per 1x128 K block, exps U{{-4..4}}, seed 4, " \
                      "swizzled group 16; time includes the per-call scale repack"
     out["mxfp8"] = mx
     del tqa, tsa, tqb, tsb
@@ -565,7 +568,14 @@ def ragged_set(torch, pgt, ctx, device):
 
 
 def main():
+    global M, N, K, FLOP, WORKLOAD
     args = parse()
+    if args.size != 8192:
+        if args.size < 256 or args.size % 256:
+            raise SystemExit("--size must be a positive multiple of 256")
+        M = N = K = args.size
+        FLOP = 2.0 * M * N * K
+        WORKLOAD = WORKLOAD.replace("M=N=K=8192", f"M=N=K={args.size}")
     world, rank, local, pg = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
