@@ -183,12 +183,14 @@ def time_launches(torch, launch, steps: int, warmup: int):
 
 
 def tail_idle(times_ns: np.ndarray) -> float:
-    """1 - sum(busy) / (P * span): the share of worker time spent idle in the launch."""
+    """1 - sum(busy) / (P * span): the share of worker time spent idle in the launch, over
+    the workers that ran (under launch control most launched workers are cancelled before
+    they start and record no times)."""
     t = times_ns[(times_ns[:, 0] > 0) & (times_ns[:, 1] > 0)]
     if len(t) == 0:
         return float("nan")
     span = float(t[:, 1].max() - t[:, 0].min())
-    return 1.0 - float((t[:, 1] - t[:, 0]).sum()) / (len(times_ns) * span) if span > 0 else 0.0
+    return 1.0 - float((t[:, 1] - t[:, 0]).sum()) / (len(t) * span) if span > 0 else 0.0
 
 
 def cpu_baseline(budget_s: float, A_bits, B_bits, rows_hint: int | None = None) -> dict:

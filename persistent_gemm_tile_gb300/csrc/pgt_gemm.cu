@@ -445,16 +445,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // a single accumulator: read all of it into registers (as bf16 pairs), hand
                 // it back to the MMA warp at once, then stage and store
                 uint32_t pk[BN / 2];
+                if (!gp.epi) {
 #pragma unroll
-                for (int c = 0; c < BN / 64; ++c) {
-                    uint32_t r0[32], r1[32];
-                    tmem_ld_32x32b_x32(tacc + c * 64, r0);
-                    tmem_ld_32x32b_x32(tacc + c * 64 + 32, r1);
-                    tmem_ld_wait();
+                    for (int c = 0; c < BN / 64; ++c) {
+                        uint32_t r0[32], r1[32];
+                        tmem_ld_32x32b_x32(tacc + c * 64, r0);
+                        tmem_ld_32x32b_x32(tacc + c * 64 + 32, r1);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        pk[32 * c + i] = cvt(r0[2 * i], r0[2 * i + 1], col0 + 64 * c + 2 * i);
-                        pk[32 * c + 16 + i] = cvt(r1[2 * i], r1[2 * i + 1], col0 + 64 * c + 32 + 2 * i);
+                        for (int i = 0; i < 16; ++i) {
+                            pk[32 * c + i] = pack_bf16x2(r0[2 * i], r0[2 * i + 1]);
+                            pk[32 * c + 16 + i] = pack_bf16x2(r1[2 * i], r1[2 * i + 1]);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < BN / 64; ++c) {
+                        uint32_t r0[32], r1[32];
+                        tmem_ld_32x32b_x32(tacc + c * 64, r0);
+                        tmem_ld_32x32b_x32(tacc + c * 64 + 32, r1);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            pk[32 * c + i] = cvt(r0[2 * i], r0[2 * i + 1], col0 + 64 * c + 2 * i);
+                            pk[32 * c + 16 + i] = cvt(r1[2 * i], r1[2 * i + 1], col0 + 64 * c + 32 + 2 * i);
+                        }
                     }
                 }
                 tc_fence_before();
