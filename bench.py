@@ -40,9 +40,9 @@ L2_NOTE = "inputs larger than L2: A+B+C = 384 MiB per GEMM > 129 MB L2; add x+y+
 GEMM_SOURCES = ["csrc/pgt_gemm.cu", "csrc/pgt_device.cuh", "csrc/pgt_sched.cuh"]
 ADD_SOURCES = ["csrc/pgt_add.cu", "csrc/pgt_device.cuh", "csrc/pgt_sched.cuh"]
 PROFILED_TRAFFIC = {
-    "gemm_bf16_2cta_256x256": (1.240241e9 + 1.28645376e8, GEMM_SOURCES, "1e09cd9d3fabe562"),
-    "gemm_mxfp8_2cta_256x256": (2.48906496e8 + 1.16763136e8, GEMM_SOURCES, "1e09cd9d3fabe562"),
-    "add_wide_8x1024": (5.36910592e8 + 2.29790976e8, ADD_SOURCES, "0ec4cdbf39d2f292"),
+    "gemm_bf16_2cta_256x256": (1.183503e9 + 1.27805696e8, GEMM_SOURCES, "4bddabe7090362e5"),
+    "gemm_mxfp8_2cta_256x256": (2.4797696e8 + 1.1755776e8, GEMM_SOURCES, "4bddabe7090362e5"),
+    "add_wide_8x1024": (5.36910336e8 + 2.2939648e8, ADD_SOURCES, "67138c7530c893b4"),
 }
 
 
