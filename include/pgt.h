@@ -198,6 +198,14 @@ int pgt_max_groups(const pgt_ctx* ctx);
  * block index, wait site. */
 int pgt_last_error(pgt_ctx* ctx, void* stream, int32_t* detail);
 
+/* Self-test of the bounded-wait path every kernel uses.  Launches one thread that waits on
+ * an mbarrier through the same bounded wait as the GEMM roles.  arrive != 0: the thread
+ * arrives first and the wait completes at once.  arrive == 0: nothing ever arrives, the
+ * wait gives up after the time limit (about one second), records PGT_ERR_TIMEOUT in the
+ * error word (role 3, site 12) and the kernel returns; pgt_last_error then reports it and
+ * the context stays usable.  Nothing faults, traps or hangs. */
+int pgt_wait_probe(pgt_ctx* ctx, int arrive, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* pgt_strerror(int status);
 

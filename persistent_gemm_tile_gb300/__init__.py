@@ -34,6 +34,7 @@ EXPORTS = (
     "pgt_preamble", "pgt_destroy", "pgt_num_sms", "pgt_max_groups", "pgt_last_error", "pgt_strerror",
     "pgt_gemm_workspace_bytes", "pgt_gemm_plan", "pgt_gemm_ex", "pgt_gemm", "pgt_gemm_host",
     "pgt_add", "pgt_add_workers", "pgt_schedule_log", "pgt_gemm_noalloc", "pgt_multi_loop", "pgt_set_release",
+    "pgt_wait_probe",
 )
 MAX_SPACES = 8
 NOALLOC_MAX_GROUPS = 16
@@ -104,6 +105,7 @@ def lib() -> ctypes.CDLL:
         L.pgt_gemm_noalloc.argtypes = [P, P, P, I64, I64, I64, I, I, I, P, P]
         L.pgt_multi_loop.argtypes = [P, P, I, I, I, I, I, P, P]
         L.pgt_set_release.argtypes = [P, P, I, P]
+        L.pgt_wait_probe.argtypes = [P, I, P]
         _lib = L
     return _lib
 
@@ -197,6 +199,10 @@ class Context:
         detail = (ctypes.c_int32 * 4)()
         rc = lib().pgt_last_error(self.handle, _stream(stream), ctypes.cast(detail, ctypes.c_void_p))
         return rc, list(detail)
+
+    def wait_probe(self, arrive: bool, stream=None) -> None:
+        """pgt_wait_probe: exercise the bounded-wait path (arrive=False makes it time out)."""
+        _check(lib().pgt_wait_probe(self.handle, int(bool(arrive)), _stream(stream)), "pgt_wait_probe")
 
     def gemm_plan(self, desc: GemmDesc) -> dict:
         info = PlanInfo()

@@ -65,6 +65,19 @@ __global__ void schedule_log_kernel(const SchedParams sp, int32_t* visits, int64
     if (times != nullptr) times[2 * w + 1] = (int64_t)globaltimer();
 }
 
+// Self-test of the bounded waits: one thread waits on an mbarrier that only `arrive` makes
+// complete.  Without it the wait gives up after the kernels' time limit, records the
+// timeout in the error word and the kernel returns.
+__global__ void wait_probe_kernel(int arrive, int* err) {
+    __shared__ __align__(8) uint64_t bar_word;
+    const uint32_t bar = smem_u32(&bar_word);
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    if (arrive) mbar_arrive(bar);
+    volatile int abort_flag = 0;
+    mbar_wait(bar, 0, &abort_flag, err, kRoleScheduler, 12);
+}
+
 int schedule_log_launch(pgt_ctx* ctx, int64_t m_blocks, int64_t n_blocks, int cluster_size, int sched_mode,
                         int group_size, int ws_groups, int num_workers, const pgt_trace* trace,
                         cudaStream_t stream) {
@@ -169,6 +182,13 @@ int pgt_set_release(pgt_ctx* ctx, const int32_t* h_flags, int n, void* stream) {
     if (cudaSetDevice(ctx->device) != cudaSuccess) return PGT_ERR_CUDA;
     return cuda_status(cudaMemcpyAsync(ctx->d_release, h_flags, sizeof(int32_t) * n, cudaMemcpyHostToDevice,
                                        static_cast<cudaStream_t>(stream)));
+}
+
+int pgt_wait_probe(pgt_ctx* ctx, int arrive, void* stream) {
+    if (ctx == nullptr) return PGT_ERR_ARG;
+    if (cudaSetDevice(ctx->device) != cudaSuccess) return PGT_ERR_CUDA;
+    wait_probe_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(arrive != 0, ctx->d_err);
+    return cuda_status(cudaGetLastError());
 }
 
 int pgt_num_sms(const pgt_ctx* ctx) { return ctx ? ctx->num_sms : PGT_ERR_ARG; }
