@@ -69,8 +69,8 @@ def parse():
                     help="headline kernel: the bf16 GEMM (default), or the persistent add / the MXFP8 GEMM "
                          "(for timing and profiling those kernels alone)")
     ap.add_argument("--no-extras", action="store_true", help="headline only")
-    ap.add_argument("--ragged", action="store_true",
-                    help="also time the ragged-tail GEMM set per scheduler, with tail idle from traces")
+    ap.add_argument("--no-ragged", action="store_true",
+                    help="skip the ragged-tail GEMM set (timed per scheduler, with tail idle from traces)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
     ap.add_argument("--size", type=int, default=8192,
                     help="M = N = K of the GEMM workloads (8192 is the benchmark; smaller sizes are for "
@@ -521,8 +521,9 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
                      "swizzled group 16; time includes the per-call scale repack"
     out["mxfp8"] = mx
     del tqa, tsa, tqb, tsb
-    if args.ragged:
+    if not args.no_ragged:
         out["ragged"] = ragged_set(torch, pgt, ctx, device)
+    out["small_256"] = small_256(torch, pgt, ctx, device)
     # end to end from pinned host memory through pgt_gemm_host: every step copies its A and B
     # host -> device, runs the GEMM and copies C back.  Two streams with two device buffer
     # sets let one step's GEMM and D2H overlap the next step's H2D (the link carries H2D and
@@ -559,6 +560,37 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
     del bufs
     # the oracle on the host cores
     out["cpu_baseline"] = cpu_baseline(args.cpu_seconds, A_host, B_host)
+
+
+def small_256(torch, pgt, ctx, device):
+    """bf16 256^3 (U[-1,1], seed 0) on 128 x 128 tiles (4 tiles, 4 workers): latency per
+    scheduler in microseconds; launch-bound, so no roofline fraction is claimed."""
+    import synthetic
+    a, b = synthetic.gemm_bf16_inputs(256, 256, 256, seed=0, dist="uniform")
+    ta = torch.from_numpy(a.view(np.int16)).to(device)
+    tb_ = torch.from_numpy(b.view(np.int16)).to(device)
+    tc = torch.empty((256, 256), dtype=torch.int16, device=device)
+    res = {}
+    for mode, name in ((pgt.BLOCKED, "blocked"), (pgt.INTERLEAVED, "interleaved"), (pgt.SWIZZLED, "swizzled"),
+                       (pgt.WORK_STEALING, "work_stealing"), (pgt.LAUNCH_CONTROL, "launch_control")):
+        d = pgt.make_desc(256, 256, 256, sched_mode=mode, group_size=2, kernel_cfg=pgt.CFG_1CTA_128x128)
+        _, per = time_launches(torch, lambda: ctx.gemm_ex(d, ta, tb_, tc), 50, 5)
+        # the same launches captured in a CUDA graph and replayed: device time per GEMM
+        reps = 50
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(reps):
+                ctx.gemm_ex(d, ta, tb_, tc)
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(5):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        res[name] = {"us_eager": 1e3 * float(np.median(per)), "us_graph": 1e3 * e0.elapsed_time(e1) / (5 * reps)}
+    return res
 
 
 def ragged_set(torch, pgt, ctx, device):

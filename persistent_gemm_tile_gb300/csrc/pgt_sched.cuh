@@ -122,14 +122,43 @@ struct Scheduler {
             if (p.release != nullptr && home != 0 &&
                 *reinterpret_cast<const volatile int*>(p.release + home) != 0)
                 return -1;
+            // home group first; once it is exhausted, steal from the following groups.  Counters
+            // only grow during a launch, so a group whose counter already reads >= its size is
+            // exhausted: the steal scan reads up to kScan counters at once (independent loads)
+            // and takes an atomic ticket only where one may be left.
+            constexpr int kScan = 8;
             while (cursor < p.ws_groups) {
-                int g = home + cursor;
-                if (g >= p.ws_groups) g -= p.ws_groups;
-                const int start = ws_group_start(g, p.tiles, p.ws_groups);
-                const int size = ws_group_start(g + 1, p.tiles, p.ws_groups) - start;
-                const int ticket = atomicAdd(p.counters + g * kCounterStride, 1);
-                if (ticket < size) return start + ticket;
-                ++cursor;
+                if (cursor == 0) {
+                    const int start = ws_group_start(home, p.tiles, p.ws_groups);
+                    const int size = ws_group_start(home + 1, p.tiles, p.ws_groups) - start;
+                    const int ticket = atomicAdd(p.counters + home * kCounterStride, 1);
+                    if (ticket < size) return start + ticket;
+                    cursor = 1;
+                    continue;
+                }
+                int seen[kScan];
+#pragma unroll
+                for (int j = 0; j < kScan; ++j) {
+                    int g = home + cursor + j;
+                    while (g >= p.ws_groups) g -= p.ws_groups;
+                    seen[j] = cursor + j < p.ws_groups
+                                  ? *reinterpret_cast<const volatile int*>(p.counters + g * kCounterStride)
+                                  : 0;
+                }
+                // invariant: seen[j] belongs to the group `cursor` points at in step j
+#pragma unroll
+                for (int j = 0; j < kScan; ++j) {
+                    if (cursor >= p.ws_groups) break;
+                    int g = home + cursor;
+                    while (g >= p.ws_groups) g -= p.ws_groups;
+                    const int start = ws_group_start(g, p.tiles, p.ws_groups);
+                    const int size = ws_group_start(g + 1, p.tiles, p.ws_groups) - start;
+                    if (seen[j] < size) {
+                        const int ticket = atomicAdd(p.counters + g * kCounterStride, 1);
+                        if (ticket < size) return start + ticket;
+                    }
+                    ++cursor;
+                }
             }
             return -1;
         }
