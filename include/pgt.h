@@ -301,8 +301,9 @@ int pgt_multi_loop(pgt_ctx* ctx, const pgt_scale_space* spaces, int n_spaces, in
 /* Run only the device tile scheduler (the same code the GEMM kernels run) over an
  * m_blocks x n_blocks grid of CTA tiles with `cluster_size` CTAs per worker, and record
  * each worker's visits in `trace` (one record list per WORKER, not per CTA).  One
- * single-thread worker per block; num_workers >= 1.  Work stealing uses the context's
- * counters like the GEMM. */
+ * single-thread worker per block; num_workers >= 1, and for PGT_LAUNCH_CONTROL exactly the
+ * tile count (one worker per tile; cancelled workers record nothing).  Work stealing uses
+ * the context's counters and release flags like the GEMM. */
 int pgt_schedule_log(pgt_ctx* ctx, int64_t m_blocks, int64_t n_blocks, int cluster_size,
                      int sched_mode, int group_size, int ws_groups, int num_workers,
                      const pgt_trace* trace, void* stream);

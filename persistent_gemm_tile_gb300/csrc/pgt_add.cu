@@ -8,6 +8,8 @@
 // stores (cache-streaming hints, data is touched once) when the rows allow it; ragged
 // tile edges fall back to scalar accesses.  The add is __fadd_rn: IEEE binary32, round to
 // nearest even, subnormals kept (the library is built without flush-to-zero).
+#include <mutex>
+
 #include "pgt_device.cuh"
 #include "pgt_internal.h"
 #include "pgt_sched.cuh"
@@ -148,11 +150,23 @@ int add_workers(const pgt_ctx* ctx, int64_t rows, int64_t cols, int tile_r, int 
     const int64_t tiles = m_tiles * n_tiles;
     if (tiles >= ((int64_t)1 << 31)) return PGT_ERR_ARG;
     if (num_workers > 0) return num_workers;
+    // resident CTAs per SM for this block size, cached per device
+    static std::mutex mu;
+    static int cache[64][8];  // [device][threads / 32 - 1], 0 = not queried yet
+    const int T = add_threads(tile_r, tile_c);  // a multiple of 32 in [32, 256]
+    const int slot = T / 32 - 1;
+    if (ctx->device < 0 || ctx->device >= 64) return PGT_ERR_ARG;
     int per_sm = 0;
-    const int T = add_threads(tile_r, tile_c);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, add_kernel<true>, T, 0) != cudaSuccess)
-        return PGT_ERR_CUDA;
-    if (per_sm < 1) per_sm = 1;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        per_sm = cache[ctx->device][slot];
+        if (per_sm == 0) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, add_kernel<true>, T, 0) != cudaSuccess)
+                return PGT_ERR_CUDA;
+            if (per_sm < 1) per_sm = 1;
+            cache[ctx->device][slot] = per_sm;
+        }
+    }
     int64_t w = (int64_t)per_sm * ctx->num_sms;
     if (w > tiles) w = tiles;
     return (int)w;

@@ -20,7 +20,8 @@
 // K x N (N contiguous) instead of N x K; MX = MXFP8 operands (E4M3 + E8M0 scales) instead
 // of bf16; TRACE = record every visit.
 #include <cuda_bf16.h>
-#include <stdio.h>
+
+#include <mutex>
 
 #include "pgt_device.cuh"
 #include "pgt_internal.h"
@@ -556,7 +557,9 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() {
+    static std::mutex mu;
     static EncodeTiledFn fn = nullptr;
+    std::lock_guard<std::mutex> lock(mu);
     if (fn == nullptr) {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -641,10 +644,12 @@ struct KernelInfo {
     int max_workers;
 };
 KernelInfo g_kinfo[kMaxDevices][kNumCfgSlots];
+std::mutex g_kinfo_mutex;
 
 int kernel_info(int device, int cfg, bool mx, bool bmn, bool tr, const CfgShape& s, KernelInfo* out) {
     if (device < 0 || device >= kMaxDevices) return PGT_ERR_ARG;
     const int slot = ((cfg * 2 + (int)mx) * 2 + (int)bmn) * 2 + (int)tr;
+    std::lock_guard<std::mutex> lock(g_kinfo_mutex);
     KernelInfo& ki = g_kinfo[device][slot];
     if (!ki.ready) {
         KernelFn k = pick_kernel(cfg, mx, bmn, tr);
