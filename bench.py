@@ -452,6 +452,22 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
         ms = float(np.median(per))
         per_cfg[cname] = {"tflops": FLOP / (ms * 1e-3) / 1e12, "ms": ms}
     out["per_cfg"] = per_cfg
+    # cuBLAS through torch.matmul on the same bf16 operands, rounds interleaved with this
+    # kernel (swizzled, group 16): a library point of comparison on the same GPU and power
+    # state, not part of the path
+    a16, b16 = dA.view(torch.bfloat16), dB.view(torch.bfloat16)
+    c16 = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+    head = desc_for(pgt.SWIZZLED)
+    lsamples = {"ours": [], "cublas": []}
+    for _ in range(6):
+        _, per = time_launches(torch, lambda: ctx.gemm_ex(head, dA, dB, dC), 10, 2)
+        lsamples["ours"].extend(per)
+        _, per = time_launches(torch, lambda: torch.matmul(a16, b16, out=c16), 10, 2)
+        lsamples["cublas"].extend(per)
+    out["vs_cublas"] = {name: {"tflops": FLOP / (float(np.median(v)) * 1e-3) / 1e12, "ms": float(np.median(v))}
+                        for name, v in lsamples.items()}
+    out["vs_cublas"]["ratio"] = out["vs_cublas"]["ours"]["tflops"] / out["vs_cublas"]["cublas"]["tflops"]
+    del c16
     # tail idle from traced launches (not timed)
     tails = {}
     for mode, name in names.items():
