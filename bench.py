@@ -69,6 +69,10 @@ def parse():
                     help="headline kernel: the bf16 GEMM (default), or the persistent add / the MXFP8 GEMM "
                          "(for timing and profiling those kernels alone)")
     ap.add_argument("--no-extras", action="store_true", help="headline only")
+    ap.add_argument("--sched", default="swizzled",
+                    choices=["blocked", "interleaved", "swizzled", "work_stealing", "blocked_grouped_m",
+                             "launch_control"], help="scheduler of the bf16 headline GEMM")
+    ap.add_argument("--group", type=int, default=16, help="group_size of the bf16 headline GEMM")
     ap.add_argument("--no-ragged", action="store_true",
                     help="skip the ragged-tail GEMM set (timed per scheduler, with tail idle from traces)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
@@ -273,7 +277,10 @@ def run_ours(args, world, rank, local, pg):
         return pgt.make_desc(M, N, K, b_layout=pgt.B_KN, sched_mode=mode, group_size=16, ws_groups=8,
                              kernel_cfg=cfg)
 
-    head = desc_for(pgt.SWIZZLED)
+    default_head = args.sched == "swizzled" and args.group == 16
+    head = desc_for(pgt.SCHED[args.sched]) if default_head else pgt.make_desc(
+        M, N, K, b_layout=pgt.B_KN, sched_mode=pgt.SCHED[args.sched], group_size=args.group, ws_groups=8,
+        kernel_cfg=args.cfg)
     plan = ctx.gemm_plan(head)
     launch = lambda: ctx.gemm_ex(head, dA, dB, dC)  # noqa: E731
     if args.kernel == "add":
@@ -313,7 +320,8 @@ def run_ours(args, world, rank, local, pg):
                    "l2": L2_NOTE, "parallelism": f"{world} independent GEMMs (one per GPU)"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
-                     "traffic": profiled_traffic("gemm_bf16_2cta_256x256") if plan["kernel_cfg"] == 4 else None,
+                     "traffic": profiled_traffic("gemm_bf16_2cta_256x256")
+                     if plan["kernel_cfg"] == 4 and default_head else None,
                      "peak_kind": ("sustained" if long_region else "burst") + f" bf16 ({peaks['source']})"},
         "gpu_launches": args.steps,
         "clocks": clk,
@@ -651,6 +659,8 @@ def main():
         M = N = K = args.size
         FLOP = 2.0 * M * N * K
         WORKLOAD = WORKLOAD.replace("M=N=K=8192", f"M=N=K={args.size}")
+    if args.sched != "swizzled" or args.group != 16:
+        WORKLOAD = WORKLOAD.replace("swizzled group_size=16", f"{args.sched} group_size={args.group}")
     world, rank, local, pg = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
