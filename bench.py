@@ -213,9 +213,29 @@ def cpu_baseline(budget_s: float, A_bits, B_bits, rows_hint: int | None = None) 
     t0 = time.perf_counter()
     OG.gemm_rows(A64, B64, True, K, N, np.arange(rows))
     dt = time.perf_counter() - t0
-    return {"value": 2.0 * rows * N * K / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"first {rows} rows of C for the {M}^3 bf16 GEMM (fp64 C loops, OpenMP over rows), "
-                      f"{dt:.1f} s; operand decode not timed"}
+    out = {"value": 2.0 * rows * N * K / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+           "sample": f"first {rows} rows of C for the {M}^3 bf16 GEMM (fp64 C loops, OpenMP over rows), "
+                     f"{dt:.1f} s; operand decode not timed"}
+    # the other oracle parts, as they stand: the fp32 add (numpy, one core) on 1024 rows of
+    # the add workload, and the static schedule enumeration of the headline GEMM
+    import synthetic
+    from oracle import add as OA
+    from oracle import schedule as OS
+    x, y = synthetic.add_inputs(1024, ADD_COLS, seed=1)
+    t0 = time.perf_counter()
+    OA.add_f32(x, y)
+    dt_add = time.perf_counter() - t0
+    grid = OS.grid_for(M, N, 128, 256, cs=2)
+    t0 = time.perf_counter()
+    OS.static_schedule(OS.SWIZZLED, grid, 76, 16)
+    dt_sched = time.perf_counter() - t0
+    out["others"] = {
+        "add_f32": {"value": 12.0 * x.size / dt_add / 1e9, "unit": "GB/s", "cores": 1,
+                    "sample": f"1024 rows x {ADD_COLS} columns of the fp32 add workload"},
+        "schedule": {"value": grid.tiles / dt_sched, "unit": "tiles/s", "cores": 1,
+                     "sample": f"swizzled G=16 visit lists, {grid.tiles} pair tiles on 76 workers"},
+    }
+    return out
 
 
 # ----------------------------------------------------------------- reference arm
