@@ -301,12 +301,12 @@ def run_ours(args, world, rank, local, pg):
     head = desc_for(pgt.SCHED[args.sched]) if default_head else pgt.make_desc(
         M, N, K, b_layout=pgt.B_KN, sched_mode=pgt.SCHED[args.sched], group_size=args.group, ws_groups=8,
         kernel_cfg=args.cfg)
-    plan = ctx.gemm_plan(head)
-    launch = lambda: ctx.gemm_ex(head, dA, dB, dC)  # noqa: E731
     if args.kernel == "add":
         return run_add_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peaks)
     if args.kernel == "mxfp8":
         return run_mx_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peaks, dC)
+    plan = ctx.gemm_plan(head)
+    launch = lambda: ctx.gemm_ex(head, dA, dB, dC)  # noqa: E731
 
     # ------------------------------------------------------------------ headline
     for _ in range(args.warmup):
@@ -547,8 +547,8 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
     tqb, tsb = torch.from_numpy(qb).to(device), torch.from_numpy(sb).to(device)
     mx = {}
     fp8_peak = 2.0 * peaks["bf16_burst"]  # fp8 dense is twice bf16 dense (4.5 vs 2.25 PFLOP/s nominal)
-    for cfg, cname in ((pgt.CFG_2CTA_256x256, "2cta_256x256"), (pgt.CFG_1CTA_128x256, "1cta_128x256"),
-                       (pgt.CFG_2CTA_256x128, "2cta_256x128")):
+    for cfg, cname in ((pgt.CFG_2CTA_256x256, "2cta_256x256"), (pgt.CFG_2CTA_256x224, "2cta_256x224"),
+                       (pgt.CFG_1CTA_128x256, "1cta_128x256"), (pgt.CFG_2CTA_256x128, "2cta_256x128")):
         d = pgt.make_desc(M, N, K, dtype=pgt.MXFP8, b_layout=pgt.B_NK, sched_mode=pgt.SWIZZLED, group_size=16,
                           kernel_cfg=cfg)
         ws = torch.empty(ctx.gemm_workspace_bytes(d), dtype=torch.uint8, device=device)

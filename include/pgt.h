@@ -92,12 +92,18 @@ extern "C" {
  *   1CTA_128x128 / 1CTA_128x256: one CTA, tcgen05 cta_group::1, M=128 MMAs.
  *   2CTA_256x128 / 2CTA_256x256: a CTA pair (cluster of 2) with cta_group::2 M=256
  *   MMAs, each CTA holding 128 rows of A and half of B's tile ([TS] 2-CTA kernel).
+ *   2CTA_256x224: MXFP8 only (bf16 returns PGT_ERR_UNSUPPORTED).  A pair tile 224 columns
+ *   wide (a cta_group::2 MMA takes N in steps of 32), so that two fp32 accumulators and
+ *   the scale columns fit in tensor memory together, and the epilogue of one tile
+ *   overlaps the next tile's MMAs.  The 256x256 MXFP8 tile has room for one accumulator
+ *   only.
  * PGT_CFG_AUTO picks the fastest configuration this build has for the dtype. */
 #define PGT_CFG_AUTO 0
 #define PGT_CFG_1CTA_128x128 1
 #define PGT_CFG_1CTA_128x256 2
 #define PGT_CFG_2CTA_256x128 3
 #define PGT_CFG_2CTA_256x256 4
+#define PGT_CFG_2CTA_256x224 5
 
 /* Epilogue options ([WS] passes a_scale / b_scale "if quantized" and marks bias TODO).
  * Reading taken here: per-tensor scales fold into one factor alpha = a_scale * b_scale and

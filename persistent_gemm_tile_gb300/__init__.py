@@ -25,6 +25,7 @@ BLOCKED, INTERLEAVED, SWIZZLED, WORK_STEALING, BLOCKED_GROUPED_M, LAUNCH_CONTROL
 SCHED = {"blocked": BLOCKED, "interleaved": INTERLEAVED, "swizzled": SWIZZLED,
          "work_stealing": WORK_STEALING, "blocked_grouped_m": BLOCKED_GROUPED_M, "launch_control": LAUNCH_CONTROL}
 CFG_AUTO, CFG_1CTA_128x128, CFG_1CTA_128x256, CFG_2CTA_256x128, CFG_2CTA_256x256 = 0, 1, 2, 3, 4
+CFG_2CTA_256x224 = 5  # MXFP8 only
 FLAG_HOST_RESET = 1
 EPI_ALPHA, EPI_BIAS = 1, 2
 VISIT_FIELDS = 4

@@ -43,6 +43,7 @@ template <> struct Stages<1, 128, true> { static constexpr int value = 5; };
 template <> struct Stages<1, 256, true> { static constexpr int value = 4; };
 template <> struct Stages<2, 128, true> { static constexpr int value = 7; };
 template <> struct Stages<2, 256, true> { static constexpr int value = 6; };
+template <> struct Stages<2, 224, true> { static constexpr int value = 6; };
 
 struct CfgShape {
     int cs, bn, stages, smem, bk;
@@ -61,6 +62,10 @@ bool cfg_shape(int cfg, int dtype, CfgShape* s) {
         case PGT_CFG_1CTA_128x256: *s = mx ? shape_of<1, 256, true>() : shape_of<1, 256, false>(); return true;
         case PGT_CFG_2CTA_256x128: *s = mx ? shape_of<2, 128, true>() : shape_of<2, 128, false>(); return true;
         case PGT_CFG_2CTA_256x256: *s = mx ? shape_of<2, 256, true>() : shape_of<2, 256, false>(); return true;
+        case PGT_CFG_2CTA_256x224:
+            if (!mx) return false;  // MXFP8 only: bf16 keeps two 256-column accumulators already
+            *s = shape_of<2, 224, true>();
+            return true;
         default: return false;
     }
 }
@@ -88,12 +93,13 @@ KernelFn pick_kernel(int cfg, bool mx, bool bmn, bool tr) {
         case PGT_CFG_1CTA_128x256: return mx ? pick_layout_trace<1, 256, true>(bmn, tr) : pick_layout_trace<1, 256, false>(bmn, tr);
         case PGT_CFG_2CTA_256x128: return mx ? pick_layout_trace<2, 128, true>(bmn, tr) : pick_layout_trace<2, 128, false>(bmn, tr);
         case PGT_CFG_2CTA_256x256: return mx ? pick_layout_trace<2, 256, true>(bmn, tr) : pick_layout_trace<2, 256, false>(bmn, tr);
+        case PGT_CFG_2CTA_256x224: return mx ? pick_layout_trace<2, 224, true>(bmn, tr) : nullptr;
         default: return nullptr;
     }
 }
 
 constexpr int kMaxDevices = 64;
-constexpr int kNumCfgSlots = 5 * 2 * 2 * 2;  // cfg x mx x bmn x trace
+constexpr int kNumCfgSlots = (PGT_CFG_2CTA_256x224 + 1) * 2 * 2 * 2;  // cfg x mx x bmn x trace
 
 // Per device and kernel: dynamic shared memory attribute set, and how many workers
 // (CTAs or CTA pairs) fit on the GPU at once.
@@ -144,21 +150,38 @@ int kernel_info(int device, int cfg, bool mx, bool bmn, bool tr, const CfgShape&
 }
 
 // Packed-scale workspace geometry: k groups of four 128-wide K blocks, 128-row blocks of
-// A and B rounded up to even counts (pairs of CTAs).
+// A and B rounded up to even counts (pairs of CTAs).  When the tile width `bn` is not a
+// multiple of 128, B's blocks are cut per tile instead: ceil(bn / 128) blocks per tile of
+// bn rows, so every tile's scales start on a block.
 struct SfGeometry {
     int kb, kgroups, ma, nb;
+    int tile_n, nbt;  // B rows per tile and 128-row blocks per tile (128 and 1: plain blocks)
     size_t bytes_a, bytes_b;
 };
 
-SfGeometry sf_geometry(int64_t M, int64_t N, int64_t K) {
+SfGeometry sf_geometry(int64_t M, int64_t N, int64_t K, int bn) {
     SfGeometry g;
     g.kb = (int)(K / 128);
     g.kgroups = (g.kb + 3) / 4;
     g.ma = (int)((cdiv64(M, 128) + 1) / 2 * 2);
-    g.nb = (int)((cdiv64(N, 128) + 1) / 2 * 2);
+    if (bn % 128 == 0) {
+        g.tile_n = 128;
+        g.nbt = 1;
+        g.nb = (int)((cdiv64(N, 128) + 1) / 2 * 2);
+    } else {
+        g.tile_n = bn;
+        g.nbt = (bn + 127) / 128;
+        g.nb = (int)(cdiv64(N, bn) * g.nbt);
+    }
     g.bytes_a = (size_t)g.kgroups * g.ma * 512;
     g.bytes_b = (size_t)g.kgroups * g.nb * 512;
     return g;
+}
+
+// The configuration PGT_CFG_AUTO stands for, per dtype.
+int resolve_cfg(int cfg, int dtype) {
+    (void)dtype;
+    return cfg == PGT_CFG_AUTO ? PGT_CFG_2CTA_256x256 : cfg;  // fastest measured for bf16 and MXFP8 alike
 }
 
 }  // namespace
@@ -178,7 +201,9 @@ int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, u
 
 size_t gemm_workspace_bytes(const pgt_gemm_desc& d) {
     if (d.dtype != PGT_MXFP8 || d.M < 1 || d.N < 1 || d.K < 128 || d.K % 128) return 0;
-    const SfGeometry g = sf_geometry(d.M, d.N, d.K);
+    CfgShape s;
+    if (!cfg_shape(resolve_cfg(d.kernel_cfg, d.dtype), d.dtype, &s)) return 0;
+    const SfGeometry g = sf_geometry(d.M, d.N, d.K, s.bn);
     return g.bytes_a + g.bytes_b;
 }
 
@@ -205,8 +230,7 @@ int gemm_plan(const pgt_ctx* ctx, const pgt_gemm_desc* in, pgt_gemm_desc* d, pgt
     if (d->dtype == PGT_MXFP8) {
         if (d->K % 128 != 0 || d->b_layout != PGT_B_NK) return PGT_ERR_ARG;
     }
-    if (d->kernel_cfg == PGT_CFG_AUTO)
-        d->kernel_cfg = PGT_CFG_2CTA_256x256;  // fastest measured for bf16 and MXFP8 alike
+    d->kernel_cfg = resolve_cfg(d->kernel_cfg, d->dtype);
     CfgShape s;
     if (!cfg_shape(d->kernel_cfg, d->dtype, &s)) return PGT_ERR_UNSUPPORTED;
     const int64_t m_blocks = cdiv64(d->M, 128);
@@ -298,6 +322,8 @@ int gemm_launch(pgt_ctx* ctx, const pgt_gemm_desc& d, const pgt_gemm_plan_info& 
     gp.epi = d.epilogue != 0;
     gp.alpha = (d.epilogue & PGT_EPI_ALPHA) ? d.alpha : 1.0f;
     gp.bias = (d.epilogue & PGT_EPI_BIAS) ? d.bias : nullptr;
+    gp.C = static_cast<uint16_t*>(C);
+    gp.ldc = d.ldc;
     gp.tr_visits = trace ? trace->visits : nullptr;
     gp.tr_max = trace ? trace->max_visits : 0;
     gp.tr_counts = trace ? trace->counts : nullptr;
@@ -327,14 +353,14 @@ int gemm_launch(pgt_ctx* ctx, const pgt_gemm_desc& d, const pgt_gemm_plan_info& 
     tsa = ta;
     tsb = ta;
     if (mx) {
-        const SfGeometry sg = sf_geometry(d.M, d.N, d.K);
+        const SfGeometry sg = sf_geometry(d.M, d.N, d.K, s.bn);
         uint32_t* wa = static_cast<uint32_t*>(workspace);
         uint32_t* wb = wa + sg.bytes_a / 4;
         const int64_t words = (int64_t)(sg.bytes_a + sg.bytes_b) / 4;
         int blocks = (int)((words + 255) / 256);
         if (blocks > 4 * ctx->num_sms) blocks = 4 * ctx->num_sms;
         sf_repack_kernel<<<blocks, 256, 0, stream>>>(sfa, sfb, (int)d.M, (int)d.N, sg.kb, sg.kgroups, sg.ma, sg.nb,
-                                                     wa, wb);
+                                                     sg.tile_n, sg.nbt, wa, wb);
         if (cudaGetLastError() != cudaSuccess) return PGT_ERR_CUDA;
         rc = encode_tmap_2d(&tsa, CU_TENSOR_MAP_DATA_TYPE_UINT32, wa, 128, (uint64_t)sg.kgroups * sg.ma, 512, 128, 1,
                             CU_TENSOR_MAP_SWIZZLE_NONE);

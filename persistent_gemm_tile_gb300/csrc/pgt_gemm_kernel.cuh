@@ -41,6 +41,8 @@ struct GemmParams {
     int epi;       // nonzero: C = alpha * acc + bias[n] before rounding
     float alpha;
     const float* bias;  // fp32[N] or nullptr
+    uint16_t* C;        // bf16 output (the last, narrower store chunk of a tile is written directly)
+    int64_t ldc;        // elements
     int32_t* tr_visits;
     int64_t tr_max;
     int32_t* tr_counts;
@@ -75,12 +77,20 @@ struct Layout {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SF_BYTES;
     static constexpr int TX_BYTES = A_BYTES + B_BYTES;             // per CTA, every stage
     static constexpr int SF_TX_BYTES = MX ? 512 + 512 * NB128 : 0;  // per CTA, every 4th stage
-    // accumulators: double buffered unless tensor memory cannot hold two plus the scales
-    static constexpr int SF_COLS = MX ? 2 * (4 + 4 * NB128) : 0;
-    static constexpr int ACC_BUFS = (2 * BN + SF_COLS <= 512) ? 2 : 1;
-    static constexpr int SFA_COL = ACC_BUFS * BN;
-    static constexpr int SFB_COL = SFA_COL + 8;
-    static constexpr int TMEM_COLS = pow2_at_least(ACC_BUFS * BN + SF_COLS);
+    // accumulators: double buffered unless tensor memory cannot hold two plus the scales.
+    // Accumulator a starts at column a * ACC_STRIDE (BN rounded up to 128).  The scales
+    // (two buffers of 4 SFA columns and two of 4 * NB128 SFB columns) follow the last
+    // accumulator, or, when the tile leaves a gap of at least 8 columns before the second
+    // accumulator, SFA sits in that gap and SFB follows the second accumulator.
+    static constexpr int ACC_STRIDE = (BN + 127) / 128 * 128;
+    static constexpr int SFA_COLS = MX ? 8 : 0;
+    static constexpr int SFB_COLS = MX ? 8 * NB128 : 0;
+    static constexpr bool SF_IN_GAP = MX && ACC_STRIDE - BN >= SFA_COLS && ACC_STRIDE + BN + SFB_COLS <= 512;
+    static constexpr int ACC_BUFS = (SF_IN_GAP || 2 * ACC_STRIDE + SFA_COLS + SFB_COLS <= 512) ? 2 : 1;
+    static constexpr int SFA_COL = SF_IN_GAP ? BN : ACC_BUFS * ACC_STRIDE;
+    static constexpr int SFB_COL = SF_IN_GAP ? ACC_STRIDE + BN : SFA_COL + SFA_COLS;
+    static constexpr int TMEM_COLS =
+        pow2_at_least(SF_IN_GAP ? SFB_COL + SFB_COLS : ACC_BUFS * ACC_STRIDE + SFA_COLS + SFB_COLS);
     static constexpr int EPI_BUFS = (STAGES * STAGE_BYTES + kEpiWarps * 2 * kEpiBufBytes + 2048 <= kMaxSmem) ? 2 : 1;
     static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
     static constexpr int BAR_OFF = EPI_OFF + kEpiWarps * EPI_BUFS * kEpiBufBytes;
@@ -97,12 +107,17 @@ struct Layout {
     static_assert(RING_OFF % 16 == 0 && MISC_OFF % 16 == 0, "ring entries are 16-byte vectors");
     static_assert(SMEM <= kMaxSmem, "dynamic shared memory above the 227 KB per-CTA limit");
     static_assert(TMEM_COLS <= 512, "tensor memory holds 512 columns");
-    static_assert(BN_CTA % 64 == 0, "B is loaded in 64-wide boxes");
+    static_assert(BN_CTA % 8 == 0, "B rows per CTA must fill whole 8-row swizzle atoms");
+    static_assert(MX || BN % 64 == 0, "bf16 tiles are whole 64-column store chunks");
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void st_global_v4(uint16_t* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -135,6 +150,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const __grid_constant__ CUtensorMap tmSFB, const GemmParams gp) {
     using L = Layout<CS, BN, STAGES, MX>;
     constexpr bool kPair = CS == 2;
+    static_assert(!B_MN || L::BN_CTA % 64 == 0, "B stored K x N is loaded in 64-column boxes");
+    static_assert(BN % 64 == 0 || L::ACC_BUFS == 2, "a ragged last store chunk needs the double-buffered epilogue");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -324,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait<kPair>(tempty(acc), ((tc / L::ACC_BUFS) & 1u) ^ 1u, abort_flag, gp.err, kRoleMma, 3))
                     break;
                 tc_fence_after();
-                const uint32_t d = tmem_base + acc * BN;
+                const uint32_t d = tmem_base + acc * L::ACC_STRIDE;
                 for (int k = 0; k < gp.k_iters; ++k, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
@@ -406,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int row0 = (e.y * CS + (int)rank) * L::BM + 32 * qw;
             const int col0 = e.z * BN;
-            const uint32_t tacc = tmem_base + ((uint32_t)(32 * qw) << 16) + acc * BN;
+            const uint32_t tacc = tmem_base + ((uint32_t)(32 * qw) << 16) + acc * L::ACC_STRIDE;
             // fp32 accumulator pair -> bf16x2, with the optional scale and bias fused in
             // (one fma per element; columns past N read no bias)
             auto cvt = [&](uint32_t lo, uint32_t hi, int col) __attribute__((always_inline)) -> uint32_t {
@@ -481,13 +498,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < BN / 64; ++c) store_chunk(c, pk + 32 * c);
             } else {
+                constexpr int kFull = BN / 64;  // whole 64-column chunks, stored through TMA
+                constexpr int kTail = BN % 64;  // columns of a narrower last chunk (MXFP8 256 x 224)
 #pragma unroll 1
-                for (int c = 0; c < BN / 64; ++c) {
+                for (int c = 0; c < kFull; ++c) {
                     uint32_t r0[32], r1[32], w[32];
                     tmem_ld_32x32b_x32(tacc + c * 64, r0);
                     tmem_ld_32x32b_x32(tacc + c * 64 + 32, r1);
                     tmem_ld_wait();
-                    if (c == BN / 64 - 1) {
+                    if (kTail == 0 && c == kFull - 1) {
                         // accumulator fully read: hand it back to the MMA warp
                         tc_fence_before();
                         __syncwarp();
@@ -499,6 +518,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                         w[16 + i] = cvt(r1[2 * i], r1[2 * i + 1], col0 + 64 * c + 32 + 2 * i);
                     }
                     store_chunk(c, w);
+                }
+                if constexpr (kTail > 0) {
+                    // The last kTail columns: read them, hand the accumulator back, and store
+                    // each thread's row segment with 16-byte global stores.  A TMA box of 64
+                    // columns would overwrite the next tile's first columns.  Rows past M and
+                    // columns past N are not written.
+                    static_assert(kTail == 16 || kTail == 32 || kTail == 48, "tail is 16, 32 or 48 columns");
+                    uint32_t ta[32], tb[16];
+                    const uint32_t tcol = tacc + kFull * 64;
+                    if constexpr (kTail == 16) {
+                        tmem_ld_32x32b_x16(tcol, tb);
+                    } else {
+                        tmem_ld_32x32b_x32(tcol, ta);
+                        if constexpr (kTail == 48) tmem_ld_32x32b_x16(tcol + 32, tb);
+                    }
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) arrive_local_or_leader(tempty(acc), !leader);
+                    auto tv = [&](int i) __attribute__((always_inline)) -> uint32_t {
+                        if constexpr (kTail == 16)
+                            return tb[i];
+                        else
+                            return i < 32 ? ta[i] : tb[i - 32];
+                    };
+                    const int row = row0 + (int)lane;
+                    const int cb = col0 + kFull * 64;
+                    if (row < gp.M) {
+                        uint16_t* dst = gp.C + (int64_t)row * gp.ldc + cb;
+#pragma unroll
+                        for (int j = 0; j < kTail / 8; ++j) {
+                            uint32_t q[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                q[i] = cvt(tv(8 * j + 2 * i), tv(8 * j + 2 * i + 1), cb + 8 * j + 2 * i);
+                            const int c8 = cb + 8 * j;
+                            if (c8 + 8 <= gp.N) {
+                                st_global_v4(dst + 8 * j, q[0], q[1], q[2], q[3]);
+                            } else {
+                                for (int e = 0; e < 8 && c8 + e < gp.N; ++e)
+                                    dst[8 * j + e] = (uint16_t)(q[e >> 1] >> (16 * (e & 1)));
+                            }
+                        }
+                    }
                 }
             }
             ++tc;
@@ -520,11 +583,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // MXFP8 scales: plain [rows][K/128] bytes -> for each group of four 128-wide K blocks and
 // each block of 128 rows, 512 bytes in the tensor-memory copy layout (byte
-// lane*16 + c*4 + j holds row c*32 + lane, K block 4*group + j; zero past the edges).
-// Output row (group * blocks + block) is one 128-word line: group-major, row-block minor.
+// lane*16 + c*4 + j holds row c*32 + lane of the block, K block 4*group + j; zero past the
+// edges).  Output row (group * blocks + block) is one 128-word line: group-major, block
+// minor.  A's blocks are plain 128-row blocks.  B's blocks are cut per tile of `tile_n` rows,
+// `nbt` blocks per tile (tile_n = 128, nbt = 1 gives plain blocks): block b of tile t covers
+// rows t*tile_n + b*128 ... up to the tile's end.
 __global__ void sf_repack_kernel(const uint8_t* __restrict__ sfa, const uint8_t* __restrict__ sfb, int M, int N,
-                                 int kb, int kgroups, int ma, int nb, uint32_t* __restrict__ outa,
-                                 uint32_t* __restrict__ outb) {
+                                 int kb, int kgroups, int ma, int nb, int tile_n, int nbt,
+                                 uint32_t* __restrict__ outa, uint32_t* __restrict__ outb) {
     const int64_t words_a = (int64_t)kgroups * ma * 128;
     const int64_t words_b = (int64_t)kgroups * nb * 128;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < words_a + words_b;
@@ -538,18 +604,21 @@ __global__ void sf_repack_kernel(const uint8_t* __restrict__ sfa, const uint8_t*
         const int64_t line = i >> 7;
         const int blk = (int)(line % blocks);
         const int kg = (int)(line / blocks);
-        const int r = blk * 128 + (w & 3) * 32 + (w >> 2);
+        const int in_block = (w & 3) * 32 + (w >> 2);
+        const int per_tile = is_a ? 1 : nbt;
+        const int span = is_a ? 128 : tile_n;
+        const int b = blk % per_tile;
+        const int64_t r = (int64_t)(blk / per_tile) * span + b * 128 + in_block;
         uint32_t v = 0;
-        if (r < rows) {
+        if (b * 128 + in_block < span && r < rows) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int kbi = kg * 4 + j;
-                if (kbi < kb) v |= (uint32_t)src[(int64_t)r * kb + kbi] << (8 * j);
+                if (kbi < kb) v |= (uint32_t)src[r * kb + kbi] << (8 * j);
             }
         }
         (is_a ? outa : outb)[i] = v;
     }
 }
-
 
 }  // namespace pgt

@@ -52,7 +52,8 @@ def test_binding_constants_match_header():
         "PGT_LAUNCH_CONTROL": pgt.LAUNCH_CONTROL,
         "PGT_CFG_AUTO": pgt.CFG_AUTO, "PGT_CFG_1CTA_128x128": pgt.CFG_1CTA_128x128,
         "PGT_CFG_1CTA_128x256": pgt.CFG_1CTA_128x256, "PGT_CFG_2CTA_256x128": pgt.CFG_2CTA_256x128,
-        "PGT_CFG_2CTA_256x256": pgt.CFG_2CTA_256x256, "PGT_FLAG_HOST_RESET": pgt.FLAG_HOST_RESET,
+        "PGT_CFG_2CTA_256x256": pgt.CFG_2CTA_256x256, "PGT_CFG_2CTA_256x224": pgt.CFG_2CTA_256x224,
+        "PGT_FLAG_HOST_RESET": pgt.FLAG_HOST_RESET,
         "PGT_VISIT_FIELDS": pgt.VISIT_FIELDS, "PGT_NOALLOC_MAX_GROUPS": pgt.NOALLOC_MAX_GROUPS,
         "PGT_EPI_ALPHA": pgt.EPI_ALPHA, "PGT_EPI_BIAS": pgt.EPI_BIAS, "PGT_MAX_SPACES": pgt.MAX_SPACES,
     }
@@ -83,6 +84,25 @@ def test_null_arguments_rejected_without_touching_a_gpu(lib):
     assert lib.pgt_preamble(0, 0, 0, ctypes.byref(h)) == pgt.ERR_ARG  # max_groups < 1
     assert lib.pgt_preamble(0, 65, 0, ctypes.byref(h)) == pgt.ERR_ARG
     assert lib.pgt_preamble(0, 8, 4, ctypes.byref(h)) == pgt.ERR_ARG  # unknown flag
+
+
+def test_mxfp8_workspace_bytes_per_configuration(lib):
+    """Packed-scale workspace: k groups of four 128-wide K blocks x (A blocks + B blocks) x
+    512 bytes.  A and B use 128-row blocks rounded up to even counts, except that for the
+    224-column pair tile B's blocks are cut per tile (two per 224-row tile)."""
+    def ws(M, N, K, cfg):
+        d = pgt.make_desc(M, N, K, dtype=pgt.MXFP8, b_layout=pgt.B_NK, kernel_cfg=cfg)
+        return lib.pgt_gemm_workspace_bytes(ctypes.byref(d))
+    even = lambda v: (v + 1) // 2 * 2  # noqa: E731
+    for M, N, K in ((8192, 8192, 8192), (1000, 1100, 1664), (128, 224, 128), (384, 448, 512)):
+        kg = (K // 128 + 3) // 4
+        ma = even(-(-M // 128))
+        for cfg in (pgt.CFG_AUTO, pgt.CFG_1CTA_128x128, pgt.CFG_2CTA_256x256):
+            assert ws(M, N, K, cfg) == kg * (ma + even(-(-N // 128))) * 512, (M, N, K, cfg)
+        assert ws(M, N, K, pgt.CFG_2CTA_256x224) == kg * (ma + 2 * -(-N // 224)) * 512, (M, N, K)
+    assert ws(8192, 8192, 8192, 99) == 0  # unknown configuration
+    d = pgt.make_desc(256, 256, 256, kernel_cfg=pgt.CFG_2CTA_256x224)  # bf16 needs none
+    assert lib.pgt_gemm_workspace_bytes(ctypes.byref(d)) == 0
 
 
 def test_oracle_and_library_share_no_code():

@@ -57,12 +57,13 @@ def test_random_scale_bias_ragged(ctx, cfg, alpha, use_bias):
     OG.check(c, Ce, Ae)
 
 
-def test_mxfp8_with_scale_and_bias(ctx):
-    M, N, K = 512, 768, 1024
+@pytest.mark.parametrize("cfg", [pgt.CFG_AUTO, pgt.CFG_2CTA_256x224])
+def test_mxfp8_with_scale_and_bias(ctx, cfg):
+    M, N, K = 512, 872, 1024  # 872 = 3 * 224 + 200: the last 224-column tile's 32-column tail holds 8
     qa, sa, qb, sb = synthetic.gemm_mxfp8_inputs(M, N, K, seed=43)
     bias = np.random.default_rng(44).uniform(-2, 2, N).astype(np.float32)
     dbias = torch.from_numpy(bias).cuda()  # the descriptor holds only its address: keep it alive
-    desc = pgt.make_desc(M, N, K, dtype=pgt.MXFP8, b_layout=pgt.B_NK, alpha=0.5, bias=dbias)
+    desc = pgt.make_desc(M, N, K, dtype=pgt.MXFP8, b_layout=pgt.B_NK, alpha=0.5, bias=dbias, kernel_cfg=cfg)
     ws = torch.zeros(ctx.gemm_workspace_bytes(desc), dtype=torch.uint8, device="cuda")
     C = torch.full((M, N), -1, dtype=torch.int16, device="cuda")
     ctx.gemm_ex(desc, dev_u8(qa), dev_u8(qb), C, sfa=dev_u8(sa), sfb=dev_u8(sb), workspace=ws)

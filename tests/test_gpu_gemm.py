@@ -237,7 +237,8 @@ def test_argument_errors(ctx):
         (dict(ws_groups=17), pgt.ERR_GROUPS),
         (dict(group_size=0), pgt.ERR_ARG),
         (dict(sched_mode=9), pgt.ERR_ARG),
-        (dict(kernel_cfg=pgt.CFG_2CTA_256x256 + 1), pgt.ERR_UNSUPPORTED),
+        (dict(kernel_cfg=99), pgt.ERR_UNSUPPORTED),
+        (dict(kernel_cfg=pgt.CFG_2CTA_256x224), pgt.ERR_UNSUPPORTED),  # MXFP8 only
         (dict(dtype=pgt.MXFP8, b_layout=pgt.B_KN), pgt.ERR_ARG),  # MXFP8 needs B stored N x K
     ]
     for kw, status in bad:

@@ -19,7 +19,8 @@ from oracle import schedule as S
 
 pytestmark = pytest.mark.gpu
 
-MX_CFGS = [pgt.CFG_1CTA_128x128, pgt.CFG_1CTA_128x256, pgt.CFG_2CTA_256x128, pgt.CFG_2CTA_256x256]
+MX_CFGS = [pgt.CFG_1CTA_128x128, pgt.CFG_1CTA_128x256, pgt.CFG_2CTA_256x128, pgt.CFG_2CTA_256x256,
+           pgt.CFG_2CTA_256x224]
 MODES = [pgt.BLOCKED, pgt.INTERLEAVED, pgt.SWIZZLED, pgt.WORK_STEALING, pgt.BLOCKED_GROUPED_M]
 
 
@@ -31,12 +32,13 @@ def ctx():
     c.close()
 
 
-def run_mx(ctx, qa, sa, qb, sb, M, N, K, cfg=pgt.CFG_AUTO, mode=pgt.SWIZZLED, G=16, workers=0, trace=False):
+def run_mx(ctx, qa, sa, qb, sb, M, N, K, cfg=pgt.CFG_AUTO, mode=pgt.SWIZZLED, G=16, workers=0, trace=False,
+           ldc=0):
     desc = pgt.make_desc(M, N, K, dtype=pgt.MXFP8, b_layout=pgt.B_NK, sched_mode=mode, group_size=G,
-                         kernel_cfg=cfg, num_workers=workers)
+                         kernel_cfg=cfg, num_workers=workers, ldc=ldc)
     plan = ctx.gemm_plan(desc)
     ws = torch.zeros(max(ctx.gemm_workspace_bytes(desc), 16), dtype=torch.uint8, device="cuda")
-    C = torch.full((M, N), -1, dtype=torch.int16, device="cuda")
+    C = torch.full((M, ldc or N), -1, dtype=torch.int16, device="cuda")
     tb = pgt.TraceBuffers(plan["ctas"], plan["tiles"]) if trace else None
     args = [qa, qb, C]
     ctx.gemm_ex(desc, *args, sfa=sa, sfb=sb, workspace=ws, trace=tb.struct if tb else None)
@@ -106,13 +108,38 @@ def test_random_modes_bit_identical_with_traces(ctx, cfg):
             assert [[(t, m, n) for (t, m, n, _) in v] for v in wv] == [[(t, m, n) for (_, t, m, n) in v] for v in want]
 
 
+@pytest.mark.parametrize("mode", MODES + [pgt.LAUNCH_CONTROL])
+def test_224_tile_ragged_tail_columns(ctx, mode):
+    """The 224-column pair tile stores its last 32 columns with direct global stores.  N =
+    1100 ends inside that tail chunk (at a column that is not a multiple of 8), M = 1000 is
+    ragged, and ldc = 1104: the padding columns must stay untouched."""
+    M, N, K, ldc = 1000, 1100, 1664, 1104
+    qa, sa, qb, sb = synthetic.gemm_mxfp8_inputs(M, N, K, seed=34)
+    C, plan, _ = run_mx(ctx, *dev(qa, sa, qb, sb), M, N, K, cfg=pgt.CFG_2CTA_256x224, mode=mode, G=2, ldc=ldc)
+    assert plan["bn"] == 224 and plan["n_blocks"] == 5
+    c = host_u16(C)
+    assert np.all(c[:, N:] == 0xFFFF)
+    C64, Abs = OG.gemm_full(OG.dequant_mxfp8(qa, sa), OG.dequant_mxfp8(qb, sb), False, M, N, K)
+    OG.check(c[:, :N], C64, Abs)
+    C2, _, _ = run_mx(ctx, *dev(qa, sa, qb, sb), M, N, K, cfg=pgt.CFG_2CTA_256x224, mode=pgt.BLOCKED, G=2, ldc=ldc)
+    assert torch.equal(C, C2)
+
+
+def test_224_tile_unsupported_for_bf16(ctx):
+    A = torch.zeros((256, 256), dtype=torch.int16, device="cuda")
+    desc = pgt.make_desc(256, 256, 256, kernel_cfg=pgt.CFG_2CTA_256x224)
+    with pytest.raises(pgt.PgtError) as e:
+        ctx.gemm_ex(desc, A, A, A)
+    assert e.value.status == pgt.ERR_UNSUPPORTED
+
+
 @pytest.fixture(scope="module")
 def big_mx():
     M = N = K = 8192
     return synthetic.gemm_mxfp8_inputs(M, N, K, seed=4)
 
 
-@pytest.mark.parametrize("cfg", [pgt.CFG_AUTO, pgt.CFG_1CTA_128x256])
+@pytest.mark.parametrize("cfg", [pgt.CFG_AUTO, pgt.CFG_1CTA_128x256, pgt.CFG_2CTA_256x224])
 def test_8192_mxfp8_swizzled_sampled_rows(ctx, big_mx, cfg):
     M = N = K = 8192
     qa, sa, qb, sb = big_mx
