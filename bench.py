@@ -598,13 +598,57 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
 
     pipelined(2)
     total = pipelined(e2e_steps)
+    h2d_b = int(hA.numel() * 2 + hB.numel() * 2)
+    d2h_b = int(hCs[0].numel() * 2)
+    link = link_bandwidth(torch, hA, dA, hCs[1], dC, streams)
+    # the link bound of one step: its H2D and D2H bytes with both directions busy at once,
+    # and never less than its H2D bytes alone (the GEMM overlaps the other stream's copies)
+    bound_ms = max((h2d_b + d2h_b) / (link["both_gbs"] * 1e9), h2d_b / (link["h2d_gbs"] * 1e9)) * 1e3
+    step_ms = total / e2e_steps
     out["e2e"] = {"value": FLOP * e2e_steps / (total * 1e-3) / 1e12, "unit": "TFLOP/s",
-                  "h2d_bytes_per_step": int(hA.numel() * 2 + hB.numel() * 2),
-                  "d2h_bytes_per_step": int(hCs[0].numel() * 2), "steps": e2e_steps, "streams": 2,
-                  "single_stream_value": FLOP * e2e_steps / (single * 1e-3) / 1e12}
+                  "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b, "steps": e2e_steps, "streams": 2,
+                  "single_stream_value": FLOP * e2e_steps / (single * 1e-3) / 1e12,
+                  "link": link, "ms_per_step": step_ms, "link_bound_ms_per_step": bound_ms,
+                  "frac_of_link_bound": bound_ms / step_ms}
     del bufs
     # the oracle on the host cores
     out["cpu_baseline"] = cpu_baseline(args.cpu_seconds, A_host, B_host)
+
+
+def link_bandwidth(torch, h_in, d_in, h_out, d_out, streams) -> dict:
+    """Host link bandwidth with pinned buffers: H2D alone, D2H alone, and both at once on two
+    streams (GB/s, best of 3).  The copy engines and kernels that load or store host memory
+    directly reach the same figures on this machine, so this is the e2e roofline."""
+    def timed(fn, nbytes):
+        best = 0.0
+        for _ in range(3):
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            best = max(best, nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
+        return best
+
+    n_in = h_in.numel() * h_in.element_size()
+    n_out = h_out.numel() * h_out.element_size()
+
+    def both():
+        ev = torch.cuda.Event()
+        ev.record()
+        for st in streams:
+            st.wait_event(ev)
+        with torch.cuda.stream(streams[0]):
+            d_in.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(streams[1]):
+            h_out.copy_(d_out, non_blocking=True)
+        for st in streams:
+            torch.cuda.current_stream().wait_stream(st)
+
+    return {"h2d_gbs": timed(lambda: d_in.copy_(h_in, non_blocking=True), n_in),
+            "d2h_gbs": timed(lambda: h_out.copy_(d_out, non_blocking=True), n_out),
+            "both_gbs": timed(both, n_in + n_out)}
 
 
 def small_256(torch, pgt, ctx, device):
