@@ -7,7 +7,7 @@ timed headline loop: TFLOP/s per scheduler mode, the persistent add's GB/s on fp
 8192 x 8192 (seed 1), tail idle per scheduler from traced launches, the end-to-end figure
 from host memory, and the CPU oracle timed on a bounded sample.
 
-``--impl reference`` times the CPU oracle (the reference arm of this build) on the same
+``--impl reference`` times the CPU oracle (the benchmark's reference arm) on the same
 workload and prints the same JSON line with ``"impl": "reference"``.
 """
 from __future__ import annotations
@@ -17,6 +17,7 @@ import json
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -102,10 +103,9 @@ class Clocks:
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"pgt_clocks_{os.getpid()}.csv")
 
     def start(self):
-        os.makedirs(os.path.dirname(self.path), exist_ok=True)
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",

@@ -43,7 +43,7 @@ extern "C" {
 #define PGT_OK 0
 #define PGT_ERR_ARG (-1)         /* null pointer, size out of range, bad enum value */
 #define PGT_ERR_ALIGN (-2)       /* base pointer or row stride not a multiple of 16 bytes */
-#define PGT_ERR_UNSUPPORTED (-3) /* valid arguments this build has no kernel for */
+#define PGT_ERR_UNSUPPORTED (-3) /* valid arguments the library has no kernel for */
 #define PGT_ERR_CUDA (-4)        /* a CUDA runtime/driver call failed */
 #define PGT_ERR_TIMEOUT (-5)     /* a device-side bounded wait ran out (from pgt_last_error) */
 #define PGT_ERR_GROUPS (-6)      /* ws_groups outside [1, max_groups] of the context */
@@ -97,7 +97,7 @@ extern "C" {
  *   the scale columns fit in tensor memory together, and the epilogue of one tile
  *   overlaps the next tile's MMAs.  The 256x256 MXFP8 tile has room for one accumulator
  *   only.
- * PGT_CFG_AUTO picks the fastest configuration this build has for the dtype. */
+ * PGT_CFG_AUTO picks the fastest configuration the library has for the dtype. */
 #define PGT_CFG_AUTO 0
 #define PGT_CFG_1CTA_128x128 1
 #define PGT_CFG_1CTA_128x256 2
