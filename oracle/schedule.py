@@ -36,12 +36,20 @@ range ``[floor(g*T/G_ws), floor((g+1)*T/G_ws))``; worker ``c`` starts at its hom
 exhausted.  Stolen tiles are decoded with the swizzled decode (linear when ``G <= 1``).
 The visit order is not deterministic, so only the properties in :func:`check_ws_trace`
 are fixed.
+
+Tile ownership ``layout``: ``WS_RANGES`` is the reading above (the page's per-XCD
+counters, each over its own contiguous range, so each XCD's L2 sees one region).
+``WS_STRIPED`` is a variant for a GPU whose L2 all groups share: group ``g`` owns the
+tiles ``t`` with ``t mod G_ws == g``, ticket ``j`` being tile ``j*G_ws + g``, so the
+groups advance together along the decode order.  Counters, homes, stealing, release and
+reset are unchanged.
 """
 from __future__ import annotations
 
 from dataclasses import dataclass
 
 BLOCKED, INTERLEAVED, SWIZZLED, WORK_STEALING, BLOCKED_GROUPED_M, LAUNCH_CONTROL = 0, 1, 2, 3, 4, 5
+WS_RANGES, WS_STRIPED = 0, 1
 MODE_NAMES = {
     BLOCKED: "blocked",
     INTERLEAVED: "interleaved",
@@ -144,12 +152,21 @@ def ws_partition(T: int, groups: int) -> list[tuple[int, int]]:
     return [(bounds[g], bounds[g + 1] - bounds[g]) for g in range(groups)]
 
 
+def ws_group_tiles(T: int, groups: int, layout: int = WS_RANGES) -> list[list[int]]:
+    """Each counter group's tiles in ticket order (ticket j is the list's j-th tile)."""
+    if layout == WS_RANGES:
+        return [list(range(s, s + n)) for s, n in ws_partition(T, groups)]
+    if layout == WS_STRIPED:
+        return [list(range(g, T, groups)) for g in range(groups)]
+    raise ValueError(f"unknown tile layout {layout}")
+
+
 class WsState:
     """Counters plus each worker's cursor: the sequential model of the ticket protocol."""
 
-    def __init__(self, T: int, P: int, groups: int):
+    def __init__(self, T: int, P: int, groups: int, layout: int = WS_RANGES):
         self.T, self.P, self.groups = T, P, groups
-        self.part = ws_partition(T, groups)
+        self.tiles = ws_group_tiles(T, groups, layout)
         self.counter = [0] * groups
         self.cursor = [0] * P  # groups already found exhausted, counted from home
         self.done = [False] * P
@@ -170,18 +187,17 @@ class WsState:
             g = (home + self.cursor[c]) % self.groups
             ticket = self.counter[g]
             self.counter[g] += 1  # the atomic add
-            start, size = self.part[g]
-            if ticket < size:
-                return start + ticket
+            if ticket < len(self.tiles[g]):
+                return self.tiles[g][ticket]
             self.cursor[c] += 1
         self.done[c] = True
         return -1
 
 
-def ws_simulate(T: int, P: int, groups: int, pick, release_at=None) -> list[list[int]]:
+def ws_simulate(T: int, P: int, groups: int, pick, release_at=None, layout: int = WS_RANGES) -> list[list[int]]:
     """Run the protocol with workers fetching in the order chosen by ``pick(live) -> c``.
     ``release_at(step) -> set of released groups`` models flags raised while it runs."""
-    st = WsState(T, P, groups)
+    st = WsState(T, P, groups, layout)
     visits: list[list[int]] = [[] for _ in range(P)]
     live = list(range(P))
     step = 0
@@ -197,7 +213,7 @@ def ws_simulate(T: int, P: int, groups: int, pick, release_at=None) -> list[list
     return visits
 
 
-def check_ws_trace(visits: list[list[int]], T: int, groups: int) -> None:
+def check_ws_trace(visits: list[list[int]], T: int, groups: int, layout: int = WS_RANGES) -> None:
     """Validate a work-stealing visit log (per worker, tile ids in visit order).
 
     Raises AssertionError unless: every tile in [0, T) is visited exactly once; inside each
@@ -206,20 +222,19 @@ def check_ws_trace(visits: list[list[int]], T: int, groups: int) -> None:
     """
     flat = sorted(t for v in visits for t in v)
     assert flat == list(range(T)), "work-stealing visits are not a permutation of the tiles"
-    part = ws_partition(T, groups)
-    owner = {}
-    for g, (s, n) in enumerate(part):
-        for t in range(s, s + n):
-            owner[t] = g
+    owner, ticket = {}, {}
+    for g, tiles in enumerate(ws_group_tiles(T, groups, layout)):
+        for j, t in enumerate(tiles):
+            owner[t], ticket[t] = g, j
     for c, v in enumerate(visits):
         home = c % groups
-        last_off, last_t = -1, -1
+        last_off, last_j = -1, -1
         for t in v:
             off = (owner[t] - home) % groups
             assert off >= last_off, f"worker {c} went back to an earlier group"
             if off == last_off:
-                assert t > last_t, f"worker {c} tickets not increasing in group {owner[t]}"
-            last_off, last_t = off, t
+                assert ticket[t] > last_j, f"worker {c} tickets not increasing in group {owner[t]}"
+            last_off, last_j = off, ticket[t]
 
 
 # --------------------------------------------------------------- fused multi-space loops

@@ -152,6 +152,71 @@ def test_ws_partition_covers_tiles():
         assert max(sizes) - min(sizes) <= 1
 
 
+def test_ws_group_tiles_hand_evaluated():
+    # T = 10 tiles on 3 counters: ranges split at floor(g*10/3) = 0, 3, 6, 10; stripes take
+    # every third tile starting at the group's index
+    assert S.ws_group_tiles(10, 3, S.WS_RANGES) == [[0, 1, 2], [3, 4, 5], [6, 7, 8, 9]]
+    assert S.ws_group_tiles(10, 3, S.WS_STRIPED) == [[0, 3, 6, 9], [1, 4, 7], [2, 5, 8]]
+    with pytest.raises(ValueError):
+        S.ws_group_tiles(10, 3, 2)
+
+
+@pytest.mark.parametrize("layout", [S.WS_RANGES, S.WS_STRIPED])
+def test_ws_group_tiles_partition_exactly_once(layout):
+    for T, G in itertools.product(range(0, 60), (1, 2, 3, 7, 8, 16)):
+        groups = S.ws_group_tiles(T, G, layout)
+        assert len(groups) == G
+        assert sorted(t for g in groups for t in g) == list(range(T))
+        sizes = [len(g) for g in groups]
+        assert max(sizes) - min(sizes) <= 1
+        assert all(g == sorted(g) for g in groups)  # tickets follow tile order
+
+
+def test_ws_striped_first_wave_is_the_static_first_wave():
+    # the reason for the striped layout: when P workers (P a multiple of G) take their first
+    # home ticket together, worker c gets tile (c div G) * G + c mod G = c, the same tiles
+    # the interleaved order runs in its first wave; contiguous ranges spread them instead
+    for P, G in ((16, 8), (76, 4), (24, 3)):
+        T = 10 * P
+        st = S.WsState(T, P, G, S.WS_STRIPED)
+        assert sorted(st.fetch(c) for c in range(P)) == list(range(P))
+        st = S.WsState(T, P, G, S.WS_RANGES)
+        assert sorted(st.fetch(c) for c in range(P)) != list(range(P))
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_ws_striped_random_interleavings_valid(seed):
+    rnd = random.Random(100 + seed)
+    T, P, G = rnd.randint(0, 300), rnd.randint(1, 20), rnd.choice([1, 2, 3, 8])
+    visits = S.ws_simulate(T, P, G, lambda live: rnd.choice(live), layout=S.WS_STRIPED)
+    S.check_ws_trace(visits, T, G, S.WS_STRIPED)
+
+
+def test_ws_striped_trace_fails_the_ranges_check():
+    # a striped log read as if groups owned ranges breaks the ticket-order rule, so the
+    # layout argument of the checker matters
+    rnd = random.Random(7)
+    visits = S.ws_simulate(200, 8, 4, lambda live: rnd.choice(live), layout=S.WS_STRIPED)
+    with pytest.raises(AssertionError):
+        S.check_ws_trace(visits, 200, 4, S.WS_RANGES)
+
+
+@pytest.mark.parametrize("plant", ["dup", "drop", "swap"])
+def test_ws_striped_checker_rejects_planted_mistakes(plant):
+    rnd = random.Random(5)
+    visits = [list(v) for v in S.ws_simulate(60, 6, 3, lambda live: rnd.choice(live), layout=S.WS_STRIPED)]
+    S.check_ws_trace(visits, 60, 3, S.WS_STRIPED)
+    c = max(range(len(visits)), key=lambda i: len(visits[i]))
+    if plant == "dup":
+        visits[c].append(visits[c][0])
+    elif plant == "drop":
+        visits[c].pop()
+    else:
+        visits[c][0], visits[c][1] = visits[c][1], visits[c][0]
+    with pytest.raises(AssertionError):
+        S.check_ws_trace(visits, 60, 3, S.WS_STRIPED)
+
+
 def test_ws_single_group_round_robin_is_interleaved():
     T, P = 37, 5
     order = itertools.cycle(range(P))
@@ -167,14 +232,12 @@ def test_ws_random_interleavings_valid(seed):
     S.check_ws_trace(visits, T, G)
 
 
-def test_ws_threads_with_atomic_counters_valid():
+@pytest.mark.parametrize("layout", [S.WS_RANGES, S.WS_STRIPED])
+def test_ws_threads_with_atomic_counters_valid(layout):
     T, P, G = 500, 12, 8
-    st = S.WsState(T, P, G)
+    st = S.WsState(T, P, G, layout)
     lock = threading.Lock()
     visits = [[] for _ in range(P)]
-
-    class AtomicState(S.WsState):
-        pass
 
     def fetch(c):
         home = c % G
@@ -183,9 +246,8 @@ def test_ws_threads_with_atomic_counters_valid():
             with lock:  # the atomic add
                 ticket = st.counter[g]
                 st.counter[g] += 1
-            s0, n = st.part[g]
-            if ticket < n:
-                return s0 + ticket
+            if ticket < len(st.tiles[g]):
+                return st.tiles[g][ticket]
             st.cursor[c] += 1
         return -1
 
@@ -201,9 +263,9 @@ def test_ws_threads_with_atomic_counters_valid():
         t.start()
     for t in th:
         t.join()
-    S.check_ws_trace(visits, T, G)
+    S.check_ws_trace(visits, T, G, layout)
     # every counter ends at or above its group size (exhausted), never below
-    assert all(st.counter[g] >= n for g, (_, n) in enumerate(st.part))
+    assert all(st.counter[g] >= len(st.tiles[g]) for g in range(G))
 
 
 def _valid_trace():
