@@ -435,11 +435,14 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
     names = {pgt.BLOCKED: "blocked", pgt.INTERLEAVED: "interleaved", pgt.SWIZZLED: "swizzled",
              pgt.WORK_STEALING: "work_stealing", pgt.BLOCKED_GROUPED_M: "blocked_grouped_m",
              pgt.LAUNCH_CONTROL: "launch_control"}
-    samples = {name: [] for name in names.values()}
-    descs = {mode: desc_for(mode) for mode in names}
+    descs = {name: desc_for(mode) for mode, name in names.items()}
+    # work stealing with striped tile ownership (counter group g owns tiles t = g mod 8)
+    descs["work_stealing_striped"] = pgt.make_desc(M, N, K, b_layout=pgt.B_KN, sched_mode=pgt.WORK_STEALING,
+                                                   group_size=16, ws_groups=8, kernel_cfg=args.cfg,
+                                                   ws_layout=pgt.WS_STRIPED)
+    samples = {name: [] for name in descs}
     for _ in range(6):
-        for mode, name in names.items():
-            d = descs[mode]
+        for name, d in descs.items():
             _, per = time_launches(torch, lambda: ctx.gemm_ex(d, dA, dB, dC), 10, 2)
             samples[name].extend(per)
     for name, per in samples.items():
@@ -447,15 +450,18 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
         tf = FLOP / (ms * 1e-3) / 1e12
         per_mode[name] = {"tflops": tf, "ms": ms, "frac_of_burst_peak": tf / peaks["bf16_burst"]}
     out["per_mode"] = per_mode
-    # work stealing with 1..16 counter groups
-    ws_sweep = {}
-    for g in (1, 2, 4, 8, 16):
-        d = pgt.make_desc(M, N, K, b_layout=pgt.B_KN, sched_mode=pgt.WORK_STEALING, group_size=16, ws_groups=g,
-                          kernel_cfg=args.cfg)
-        _, per = time_launches(torch, lambda: ctx.gemm_ex(d, dA, dB, dC), 40, 5)
-        ms = float(np.median(per))
-        ws_sweep[f"groups_{g}"] = {"tflops": FLOP / (ms * 1e-3) / 1e12, "ms": ms}
-    out["work_stealing_groups"] = ws_sweep
+    # work stealing with 1..16 counter groups, contiguous ranges and striped ownership,
+    # interleaved rounds
+    wdescs = {f"{lay}_groups_{g}": pgt.make_desc(M, N, K, b_layout=pgt.B_KN, sched_mode=pgt.WORK_STEALING,
+                                                 group_size=16, ws_groups=g, kernel_cfg=args.cfg, ws_layout=code)
+              for lay, code in (("ranges", pgt.WS_RANGES), ("striped", pgt.WS_STRIPED)) for g in (1, 2, 4, 8, 16)}
+    wsamples = {k: [] for k in wdescs}
+    for _ in range(4):
+        for k, d in wdescs.items():
+            _, per = time_launches(torch, lambda: ctx.gemm_ex(d, dA, dB, dC), 10, 2)
+            wsamples[k].extend(per)
+    out["work_stealing_groups"] = {k: {"tflops": FLOP / (float(np.median(v)) * 1e-3) / 1e12,
+                                       "ms": float(np.median(v))} for k, v in wsamples.items()}
     # swizzle group width (column blocks per group), interleaved rounds
     gsamples = {g: [] for g in (2, 4, 8, 16, 32)}
     gdescs = {g: pgt.make_desc(M, N, K, b_layout=pgt.B_KN, sched_mode=pgt.SWIZZLED, group_size=g,
@@ -499,8 +505,7 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
     del c16
     # tail idle from traced launches (not timed)
     tails = {}
-    for mode, name in names.items():
-        d = desc_for(mode)
+    for name, d in descs.items():
         plan = ctx.gemm_plan(d)
         tb = pgt.TraceBuffers(plan["ctas"], plan["tiles"], device=device)
         ctx.gemm_ex(d, dA, dB, dC, trace=tb.struct)
@@ -697,10 +702,12 @@ def ragged_set(torch, pgt, ctx, device):
         tc = torch.empty((m, n), dtype=torch.int16, device=device)
         key = f"{m}x{n}x{k}"
         res[key] = {}
+        variants = [(mode, name, pgt.WS_RANGES) for mode, name in names.items()]
+        variants.append((pgt.WORK_STEALING, "work_stealing_striped", pgt.WS_STRIPED))
         for cfg, cname in ((pgt.CFG_1CTA_128x256, "1cta_128x256"), (pgt.CFG_2CTA_256x128, "2cta_256x128")):
-            for mode, name in names.items():
+            for mode, name, layout in variants:
                 d = pgt.make_desc(m, n, k, b_layout=pgt.B_KN, sched_mode=mode, group_size=16, ws_groups=8,
-                                  kernel_cfg=cfg)
+                                  kernel_cfg=cfg, ws_layout=layout)
                 _, per = time_launches(torch, lambda: ctx.gemm_ex(d, ta, tb_, tc), 20, 3)
                 ms = float(np.median(per))
                 plan = ctx.gemm_plan(d)

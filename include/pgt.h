@@ -68,9 +68,10 @@ extern "C" {
  *   SWIZZLED:          interleaved waves (tile = P*w + p, [TS]) with the group_size
  *                      column-group decode and 2-CTA pairing ([TS]).
  *   WORK_STEALING:     tiles handed out through per-group atomic counters; ws_groups
- *                      counters, group g owns tiles [g*T/G, (g+1)*T/G); a worker starts at
- *                      group (p mod G) and steals from the following groups ([WS]);
- *                      tiles decoded like SWIZZLED (linear when group_size == 1).
+ *                      counters, group g owns tiles [g*T/G, (g+1)*T/G) (or, with
+ *                      PGT_WS_STRIPED, the tiles t = g mod G); a worker starts at group
+ *                      (p mod G) and steals from the following groups ([WS]); tiles
+ *                      decoded like SWIZZLED (linear when group_size == 1).
  *   BLOCKED_GROUPED_M: blocked order with the L2-grouping decode, bands of group_size
  *                      tile rows ([PK] "PERSISTENT BLOCKED WITH L2 GROUPING").
  * P is the number of persistent workers (CTAs, or CTA pairs for 2-CTA kernels) and
@@ -119,6 +120,16 @@ extern "C" {
 /* Visit-record fields written by traced launches (int32 each). */
 #define PGT_VISIT_FIELDS 4 /* tile_id, m_idx, n_idx, smid */
 
+/* Which tiles each work-stealing counter group owns (ticket j of group g is its j-th tile).
+ *   RANGES:  the contiguous range [g*T/G, (g+1)*T/G) ([WS]: one counter per XCD, each XCD
+ *            with its own L2 working on its own region).
+ *   STRIPED: tiles g, g+G, g+2G, ...: every group advances along the same front of the
+ *            decode order, so the tiles in flight are the ones a static schedule would run
+ *            at that time.  This suits a GPU whose L2 all SMs share.  Counters, homes,
+ *            stealing, release and reset are the same. */
+#define PGT_WS_RANGES 0
+#define PGT_WS_STRIPED 1
+
 typedef struct pgt_ctx pgt_ctx;
 
 /* Full description of one GEMM C = A . B.  Leading dimensions are in elements; 0 means
@@ -136,7 +147,7 @@ typedef struct pgt_gemm_desc {
     int32_t num_workers; /* persistent workers; 0 = one per SM (pair), capped at T */
     int32_t epilogue;    /* 0, or PGT_EPI_ALPHA | PGT_EPI_BIAS */
     float alpha;         /* with PGT_EPI_ALPHA: C = alpha * (A . B) [+ bias] */
-    int32_t reserved;
+    int32_t ws_layout;   /* PGT_WS_RANGES | PGT_WS_STRIPED (work stealing only) */
     const float* bias;   /* with PGT_EPI_BIAS: DEVICE fp32[N], added to every row of C */
 } pgt_gemm_desc;
 
@@ -309,9 +320,9 @@ int pgt_multi_loop(pgt_ctx* ctx, const pgt_scale_space* spaces, int n_spaces, in
  * each worker's visits in `trace` (one record list per WORKER, not per CTA).  One
  * single-thread worker per block; num_workers >= 1, and for PGT_LAUNCH_CONTROL exactly the
  * tile count (one worker per tile; cancelled workers record nothing).  Work stealing uses
- * the context's counters and release flags like the GEMM. */
+ * the context's counters and release flags like the GEMM, with ws_layout a PGT_WS_*. */
 int pgt_schedule_log(pgt_ctx* ctx, int64_t m_blocks, int64_t n_blocks, int cluster_size,
-                     int sched_mode, int group_size, int ws_groups, int num_workers,
+                     int sched_mode, int group_size, int ws_groups, int ws_layout, int num_workers,
                      const pgt_trace* trace, void* stream);
 
 /* ------------------------------------------------------ allocation-free GEMM */

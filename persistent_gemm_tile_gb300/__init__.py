@@ -26,6 +26,7 @@ SCHED = {"blocked": BLOCKED, "interleaved": INTERLEAVED, "swizzled": SWIZZLED,
          "work_stealing": WORK_STEALING, "blocked_grouped_m": BLOCKED_GROUPED_M, "launch_control": LAUNCH_CONTROL}
 CFG_AUTO, CFG_1CTA_128x128, CFG_1CTA_128x256, CFG_2CTA_256x128, CFG_2CTA_256x256 = 0, 1, 2, 3, 4
 CFG_2CTA_256x224 = 5  # MXFP8 only
+WS_RANGES, WS_STRIPED = 0, 1
 FLAG_HOST_RESET = 1
 EPI_ALPHA, EPI_BIAS = 1, 2
 VISIT_FIELDS = 4
@@ -47,7 +48,7 @@ class GemmDesc(ctypes.Structure):
                 ("dtype", ctypes.c_int32), ("b_layout", ctypes.c_int32), ("sched_mode", ctypes.c_int32),
                 ("group_size", ctypes.c_int32), ("ws_groups", ctypes.c_int32), ("kernel_cfg", ctypes.c_int32),
                 ("num_workers", ctypes.c_int32), ("epilogue", ctypes.c_int32), ("alpha", ctypes.c_float),
-                ("reserved", ctypes.c_int32), ("bias", ctypes.c_void_p)]
+                ("ws_layout", ctypes.c_int32), ("bias", ctypes.c_void_p)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -102,7 +103,7 @@ def lib() -> ctypes.CDLL:
         L.pgt_gemm_host.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
         L.pgt_add.argtypes = [P, P, P, P, I64, I64, I64, I64, I64, I, I, I, I, P, P]
         L.pgt_add_workers.argtypes = [P, I64, I64, I, I, I]
-        L.pgt_schedule_log.argtypes = [P, I64, I64, I, I, I, I, I, P, P]
+        L.pgt_schedule_log.argtypes = [P, I64, I64, I, I, I, I, I, I, P, P]
         L.pgt_gemm_noalloc.argtypes = [P, P, P, I64, I64, I64, I, I, I, P, P]
         L.pgt_multi_loop.argtypes = [P, P, I, I, I, I, I, P, P]
         L.pgt_set_release.argtypes = [P, P, I, P]
@@ -142,7 +143,8 @@ def _stream(stream) -> int | None:
 
 
 def make_desc(M, N, K, *, lda=0, ldb=0, ldc=0, dtype=BF16, b_layout=B_KN, sched_mode=SWIZZLED,
-              group_size=16, ws_groups=0, kernel_cfg=CFG_AUTO, num_workers=0, alpha=None, bias=None) -> GemmDesc:
+              group_size=16, ws_groups=0, kernel_cfg=CFG_AUTO, num_workers=0, alpha=None, bias=None,
+              ws_layout=WS_RANGES) -> GemmDesc:
     """A pgt_gemm_desc; alpha (a_scale * b_scale) and bias (device fp32[N]) enable the epilogue.
 
     The descriptor stores only the bias tensor's address: keep the tensor alive until the
@@ -151,7 +153,7 @@ def make_desc(M, N, K, *, lda=0, ldb=0, ldc=0, dtype=BF16, b_layout=B_KN, sched_
         sched_mode = SCHED[sched_mode]
     epi = (EPI_ALPHA if alpha is not None else 0) | (EPI_BIAS if bias is not None else 0)
     return GemmDesc(M, N, K, lda, ldb, ldc, dtype, b_layout, sched_mode, group_size, ws_groups, kernel_cfg,
-                    num_workers, epi, 1.0 if alpha is None else float(alpha), 0, _ptr(bias))
+                    num_workers, epi, 1.0 if alpha is None else float(alpha), ws_layout, _ptr(bias))
 
 
 def gemm_noalloc(A, B, C, M, N, K, b_layout=B_KN, group_size=16, ws_groups=0, err=None, stream=None) -> None:
@@ -269,11 +271,11 @@ class Context:
                       "pgt_add_workers")
 
     def schedule_log(self, m_blocks, n_blocks, cluster_size, sched_mode, group_size, ws_groups, num_workers,
-                     trace: Trace, stream=None) -> None:
+                     trace: Trace, stream=None, ws_layout=WS_RANGES) -> None:
         if isinstance(sched_mode, str):
             sched_mode = SCHED[sched_mode]
         _check(lib().pgt_schedule_log(self.handle, m_blocks, n_blocks, cluster_size, sched_mode, group_size,
-                                      ws_groups, num_workers, ctypes.byref(trace), _stream(stream)),
+                                      ws_groups, ws_layout, num_workers, ctypes.byref(trace), _stream(stream)),
                "pgt_schedule_log")
 
 

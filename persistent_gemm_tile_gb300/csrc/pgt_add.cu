@@ -205,6 +205,7 @@ int add_launch(pgt_ctx* ctx, const float* x, const float* y, float* out, int64_t
     p.sp.mode = sched_mode;
     p.sp.group = 1;
     p.sp.ws_groups = 1;
+    p.sp.ws_layout = 0;
     p.sp.workers = workers;
     p.sp.counters = nullptr;
     p.sp.done = nullptr;

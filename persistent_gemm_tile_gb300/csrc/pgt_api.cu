@@ -79,7 +79,7 @@ __global__ void wait_probe_kernel(int arrive, int* err) {
 }
 
 int schedule_log_launch(pgt_ctx* ctx, int64_t m_blocks, int64_t n_blocks, int cluster_size, int sched_mode,
-                        int group_size, int ws_groups, int num_workers, const pgt_trace* trace,
+                        int group_size, int ws_groups, int ws_layout, int num_workers, const pgt_trace* trace,
                         cudaStream_t stream) {
     if (ctx == nullptr || trace == nullptr || trace->visits == nullptr || trace->counts == nullptr ||
         trace->max_visits < 1)
@@ -88,6 +88,7 @@ int schedule_log_launch(pgt_ctx* ctx, int64_t m_blocks, int64_t n_blocks, int cl
     if (sched_mode < PGT_BLOCKED || sched_mode > PGT_LAUNCH_CONTROL || group_size < 1 || num_workers < 1)
         return PGT_ERR_ARG;
     if (ws_groups < 1 || ws_groups > ctx->max_groups) return PGT_ERR_GROUPS;
+    if (ws_layout != PGT_WS_RANGES && ws_layout != PGT_WS_STRIPED) return PGT_ERR_ARG;
     const int64_t m_tiles = (m_blocks + cluster_size - 1) / cluster_size;
     const int64_t tiles = m_tiles * n_blocks;
     if (m_blocks >= ((int64_t)1 << 31) || n_blocks >= ((int64_t)1 << 31) || tiles >= ((int64_t)1 << 31))
@@ -106,6 +107,7 @@ int schedule_log_launch(pgt_ctx* ctx, int64_t m_blocks, int64_t n_blocks, int cl
     }
     sp.group = g;
     sp.ws_groups = ws_groups;
+    sp.ws_layout = ws_layout;
     sp.workers = num_workers;
     sp.counters = ctx->d_counters;
     sp.done = ctx->d_done;
@@ -317,10 +319,11 @@ int pgt_add_workers(const pgt_ctx* ctx, int64_t rows, int64_t cols, int tile_r, 
 }
 
 int pgt_schedule_log(pgt_ctx* ctx, int64_t m_blocks, int64_t n_blocks, int cluster_size, int sched_mode,
-                     int group_size, int ws_groups, int num_workers, const pgt_trace* trace, void* stream) {
+                     int group_size, int ws_groups, int ws_layout, int num_workers, const pgt_trace* trace,
+                     void* stream) {
     if (ctx == nullptr) return PGT_ERR_ARG;
     if (cudaSetDevice(ctx->device) != cudaSuccess) return PGT_ERR_CUDA;
-    return schedule_log_launch(ctx, m_blocks, n_blocks, cluster_size, sched_mode, group_size, ws_groups,
+    return schedule_log_launch(ctx, m_blocks, n_blocks, cluster_size, sched_mode, group_size, ws_groups, ws_layout,
                                num_workers, trace, static_cast<cudaStream_t>(stream));
 }
 

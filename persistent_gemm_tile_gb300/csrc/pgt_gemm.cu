@@ -219,6 +219,7 @@ int gemm_plan(const pgt_ctx* ctx, const pgt_gemm_desc* in, pgt_gemm_desc* d, pgt
     if (d->num_workers < 0) return PGT_ERR_ARG;
     if (d->ws_groups == 0) d->ws_groups = ctx->max_groups < 8 ? ctx->max_groups : 8;
     if (d->ws_groups < 1 || d->ws_groups > ctx->max_groups) return PGT_ERR_GROUPS;
+    if (d->ws_layout != PGT_WS_RANGES && d->ws_layout != PGT_WS_STRIPED) return PGT_ERR_ARG;
     const int64_t es = d->dtype == PGT_BF16 ? 2 : 1;
     const int64_t b_inner = d->b_layout == PGT_B_KN ? d->N : d->K;
     if (d->lda == 0) d->lda = d->K;
@@ -312,6 +313,7 @@ int gemm_launch(pgt_ctx* ctx, const pgt_gemm_desc& d, const pgt_gemm_plan_info& 
     }
     gp.sp.group = g;
     gp.sp.ws_groups = d.ws_groups;
+    gp.sp.ws_layout = d.ws_layout;
     gp.sp.workers = plan.workers;
     gp.sp.counters = ctx->d_counters;
     gp.sp.done = ctx->d_done;

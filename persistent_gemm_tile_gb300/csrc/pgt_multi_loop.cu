@@ -178,6 +178,7 @@ extern "C" int pgt_multi_loop(pgt_ctx* ctx, const pgt_scale_space* spaces, int n
     p.sched.mode = sched_mode;
     p.sched.group = 1;
     p.sched.ws_groups = 1;
+    p.sched.ws_layout = 0;
     p.sched.workers = workers;
     p.sched.counters = nullptr;
     p.sched.done = nullptr;

@@ -28,6 +28,7 @@ struct SchedParams {
     int mode;       // kBlocked .. kBlockedGroupedM
     int group;      // group width, already clamped to the grid (>= 1)
     int ws_groups;  // counter groups (>= 1)
+    int ws_layout;  // tile ownership of the counter groups: 0 ranges, 1 striped
     int workers;    // P
     int* counters;  // ws_groups * kCounterStride ints, zero at launch
     int* done;      // workers that have finished fetching
@@ -83,6 +84,20 @@ __device__ __forceinline__ int ws_group_start(int g, int T, int G) {
     return static_cast<int>((static_cast<long long>(g) * T) / G);
 }
 
+// Tiles owned by counter group g, and the tile its ticket j stands for.  Ranges: the
+// contiguous [g*T/G, (g+1)*T/G) (one region per group, as the per-XCD counters of the
+// tritonBLAS PR).  Striped: g, g+G, g+2G, ... (every group on the same front of the
+// decode order: one shared L2).
+__device__ __forceinline__ int ws_group_size(int g, int T, int G, int layout) {
+    if (layout == 1) return T / G + (g < T % G ? 1 : 0);
+    return ws_group_start(g + 1, T, G) - ws_group_start(g, T, G);
+}
+
+__device__ __forceinline__ int ws_group_tile(int g, int ticket, int T, int G, int layout) {
+    if (layout == 1) return ticket * G + g;
+    return ws_group_start(g, T, G) + ticket;
+}
+
 // Per-worker scheduler.  Static modes are pure functions of (worker, iteration); work
 // stealing draws tickets from the counters.
 struct Scheduler {
@@ -129,10 +144,9 @@ struct Scheduler {
             constexpr int kScan = 8;
             while (cursor < p.ws_groups) {
                 if (cursor == 0) {
-                    const int start = ws_group_start(home, p.tiles, p.ws_groups);
-                    const int size = ws_group_start(home + 1, p.tiles, p.ws_groups) - start;
+                    const int size = ws_group_size(home, p.tiles, p.ws_groups, p.ws_layout);
                     const int ticket = atomicAdd(p.counters + home * kCounterStride, 1);
-                    if (ticket < size) return start + ticket;
+                    if (ticket < size) return ws_group_tile(home, ticket, p.tiles, p.ws_groups, p.ws_layout);
                     cursor = 1;
                     continue;
                 }
@@ -151,11 +165,10 @@ struct Scheduler {
                     if (cursor >= p.ws_groups) break;
                     int g = home + cursor;
                     while (g >= p.ws_groups) g -= p.ws_groups;
-                    const int start = ws_group_start(g, p.tiles, p.ws_groups);
-                    const int size = ws_group_start(g + 1, p.tiles, p.ws_groups) - start;
+                    const int size = ws_group_size(g, p.tiles, p.ws_groups, p.ws_layout);
                     if (seen[j] < size) {
                         const int ticket = atomicAdd(p.counters + g * kCounterStride, 1);
-                        if (ticket < size) return start + ticket;
+                        if (ticket < size) return ws_group_tile(g, ticket, p.tiles, p.ws_groups, p.ws_layout);
                     }
                     ++cursor;
                 }

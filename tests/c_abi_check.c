@@ -7,6 +7,7 @@
  *                     pseudo-random data, the add, pgt_last_error, destroy
  */
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 #include <stdio.h>
 #include <stdlib.h>
@@ -30,6 +31,13 @@ static uint16_t bf16_of(float f) { /* round to nearest even; finite inputs only 
 }
 
 static int cpu_checks(void) {
+    /* the descriptor layout the C compiler uses, for the binding to compare with its own */
+    printf("layout pgt_gemm_desc %zu dtype %zu ws_groups %zu epilogue %zu alpha %zu ws_layout %zu bias %zu\n",
+           sizeof(pgt_gemm_desc), offsetof(pgt_gemm_desc, dtype), offsetof(pgt_gemm_desc, ws_groups),
+           offsetof(pgt_gemm_desc, epilogue), offsetof(pgt_gemm_desc, alpha), offsetof(pgt_gemm_desc, ws_layout),
+           offsetof(pgt_gemm_desc, bias));
+    printf("layout pgt_gemm_plan_info %zu pgt_trace %zu pgt_scale_space %zu\n", sizeof(pgt_gemm_plan_info),
+           sizeof(pgt_trace), sizeof(pgt_scale_space));
     pgt_ctx* ctx = (pgt_ctx*)0x1;
     expect("preamble null out", pgt_preamble(0, 8, 0, NULL), PGT_ERR_ARG);
     expect("preamble groups 0", pgt_preamble(0, 0, 0, &ctx), PGT_ERR_ARG);

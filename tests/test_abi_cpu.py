@@ -53,7 +53,7 @@ def test_binding_constants_match_header():
         "PGT_CFG_AUTO": pgt.CFG_AUTO, "PGT_CFG_1CTA_128x128": pgt.CFG_1CTA_128x128,
         "PGT_CFG_1CTA_128x256": pgt.CFG_1CTA_128x256, "PGT_CFG_2CTA_256x128": pgt.CFG_2CTA_256x128,
         "PGT_CFG_2CTA_256x256": pgt.CFG_2CTA_256x256, "PGT_CFG_2CTA_256x224": pgt.CFG_2CTA_256x224,
-        "PGT_FLAG_HOST_RESET": pgt.FLAG_HOST_RESET,
+        "PGT_FLAG_HOST_RESET": pgt.FLAG_HOST_RESET, "PGT_WS_RANGES": pgt.WS_RANGES, "PGT_WS_STRIPED": pgt.WS_STRIPED,
         "PGT_VISIT_FIELDS": pgt.VISIT_FIELDS, "PGT_NOALLOC_MAX_GROUPS": pgt.NOALLOC_MAX_GROUPS,
         "PGT_EPI_ALPHA": pgt.EPI_ALPHA, "PGT_EPI_BIAS": pgt.EPI_BIAS, "PGT_MAX_SPACES": pgt.MAX_SPACES,
     }

@@ -29,6 +29,25 @@ def test_c_caller_argument_checks(exe):
     assert "cpu checks: ok" in r.stdout
 
 
+def test_struct_layouts_agree_with_the_c_compiler(exe):
+    import ctypes
+
+    import persistent_gemm_tile_gb300 as pgt
+    out = subprocess.run([exe, "cpu"], capture_output=True, text=True, timeout=120).stdout
+    lines = {ln.split()[1]: ln.split()[2:] for ln in out.splitlines() if ln.startswith("layout ")}
+    desc = lines["pgt_gemm_desc"]
+    c_layout = {"size": int(desc[0])}
+    c_layout.update({desc[i]: int(desc[i + 1]) for i in range(1, len(desc), 2)})
+    py = {"size": ctypes.sizeof(pgt.GemmDesc)}
+    py.update({f: getattr(pgt.GemmDesc, f).offset for f in ("dtype", "ws_groups", "epilogue", "alpha", "ws_layout",
+                                                            "bias")})
+    assert py == c_layout
+    other = lines["pgt_gemm_plan_info"]
+    assert int(other[0]) == ctypes.sizeof(pgt.PlanInfo)
+    assert int(other[2]) == ctypes.sizeof(pgt.Trace)
+    assert int(other[4]) == ctypes.sizeof(pgt.ScaleSpace)
+
+
 @pytest.mark.gpu
 def test_c_caller_gemm_and_add_on_gpu(exe):
     r = subprocess.run([exe, "gpu"], capture_output=True, text=True, timeout=300)
