@@ -4,7 +4,8 @@
  *   c_abi_check cpu   argument checks that need no GPU (exit 0 when all statuses match)
  *   c_abi_check gpu   preamble, an all-ones GEMM (every element must equal K exactly, in
  *                     every scheduler mode), bit-identical outputs across modes on
- *                     pseudo-random data, the add, pgt_last_error, destroy
+ *                     pseudo-random data (also striped work stealing through the
+ *                     descriptor form), the add, pgt_last_error, destroy
  */
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -97,6 +98,18 @@ static int gpu_checks(void) {
             printf("FAIL mode %d differs from blocked\n", modes[m]);
             ++failures;
         }
+    }
+    /* the descriptor form: work stealing with striped tile ownership, same bits */
+    {
+        pgt_gemm_desc dd;
+        memset(&dd, 0, sizeof(dd));
+        dd.M = M; dd.N = N; dd.K = K; dd.dtype = PGT_BF16; dd.b_layout = PGT_B_KN;
+        dd.sched_mode = PGT_WORK_STEALING; dd.group_size = 16; dd.ws_groups = 4; dd.ws_layout = PGT_WS_STRIPED;
+        expect("gemm_ex striped", pgt_gemm_ex(ctx, &dd, dA, dB, NULL, NULL, dC, NULL, 0, NULL, NULL), PGT_OK);
+        cudaMemcpy(hC, dC, sizeof(uint16_t) * M * N, cudaMemcpyDeviceToHost);
+        if (memcmp(hR, hC, sizeof(uint16_t) * M * N) != 0) { printf("FAIL striped work stealing differs\n"); ++failures; }
+        dd.ws_layout = 7;
+        expect("gemm_ex bad layout", pgt_gemm_ex(ctx, &dd, dA, dB, NULL, NULL, dC, NULL, 0, NULL, NULL), PGT_ERR_ARG);
     }
     /* entries against a direct sum: every product is a multiple of 2^-8 below 2^-2 in size and
      * |sum| <= 64, so each fp32 partial sum is exact and C is that sum rounded once to bf16 */
