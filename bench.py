@@ -41,9 +41,9 @@ L2_NOTE = "inputs larger than L2: A+B+C = 384 MiB per GEMM > 129 MB L2; add x+y+
 GEMM_SOURCES = ["csrc/pgt_gemm_kernel.cuh", "csrc/pgt_device.cuh", "csrc/pgt_sched.cuh"]
 ADD_SOURCES = ["csrc/pgt_add.cu", "csrc/pgt_device.cuh", "csrc/pgt_sched.cuh"]
 PROFILED_TRAFFIC = {
-    "gemm_bf16_2cta_256x256": (1.187777e9 + 1.271744e8, GEMM_SOURCES, "80c910c6509a9775"),
-    "gemm_mxfp8_2cta_256x256": (2.50103808e8 + 1.16869888e8, GEMM_SOURCES, "80c910c6509a9775"),
-    "add_wide_8x1024": (5.36977408e8 + 2.30289152e8, ADD_SOURCES, "7ba776d0d745d9c2"),
+    "gemm_bf16_2cta_256x256": (1.197656e+09 + 1.281603e+08, GEMM_SOURCES, "c6efaff8e95d97c6"),
+    "gemm_mxfp8_2cta_256x256": (2.543516e+08 + 1.166008e+08, GEMM_SOURCES, "c6efaff8e95d97c6"),
+    "add_wide_8x1024": (5.369321e+08 + 2.292219e+08, ADD_SOURCES, "ba6a4f5c86e81ce0"),
 }
 
 
