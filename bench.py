@@ -186,6 +186,25 @@ def time_launches(torch, launch, steps: int, warmup: int):
     return evs[0].elapsed_time(evs[-1]), per
 
 
+def time_sustained(torch, launch, seconds: float, block: int = 50) -> list:
+    """Launch back to back for about `seconds`, with CUDA events every `block` launches on
+    the current stream; returns the mean per-launch ms of each block."""
+    for _ in range(3):
+        launch()
+    torch.cuda.synchronize()
+    out = []
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(block):
+            launch()
+        b.record()
+        b.synchronize()
+        out.append(a.elapsed_time(b) / block)
+    return out
+
+
 def tail_idle(times_ns: np.ndarray) -> float:
     """1 - sum(busy) / (P * span): the share of worker time spent idle in the launch, over
     the workers that ran (under launch control most launched workers are cancelled before
@@ -429,8 +448,9 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
     import synthetic
     A_host = dA.cpu().numpy().view(np.uint16)
     B_host = dB.cpu().numpy().view(np.uint16)
-    # per scheduler mode: rounds of 10 launches per mode, modes interleaved so that each sees
-    # the same mix of power and clock states; median per-launch time
+    # per scheduler mode: 1-second back-to-back loops, modes interleaved over 3 rounds so that
+    # each sees the same mix of power and clock states (the GPU is power-capped within a
+    # fraction of a second); median of the 50-launch block means
     per_mode = {}
     names = {pgt.BLOCKED: "blocked", pgt.INTERLEAVED: "interleaved", pgt.SWIZZLED: "swizzled",
              pgt.WORK_STEALING: "work_stealing", pgt.BLOCKED_GROUPED_M: "blocked_grouped_m",
@@ -441,25 +461,23 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
                                                    group_size=16, ws_groups=8, kernel_cfg=args.cfg,
                                                    ws_layout=pgt.WS_STRIPED)
     samples = {name: [] for name in descs}
-    for _ in range(6):
+    for _ in range(3):
         for name, d in descs.items():
-            _, per = time_launches(torch, lambda: ctx.gemm_ex(d, dA, dB, dC), 10, 2)
-            samples[name].extend(per)
+            samples[name].extend(time_sustained(torch, lambda: ctx.gemm_ex(d, dA, dB, dC), 1.0))
     for name, per in samples.items():
         ms = float(np.median(per))
         tf = FLOP / (ms * 1e-3) / 1e12
         per_mode[name] = {"tflops": tf, "ms": ms, "frac_of_burst_peak": tf / peaks["bf16_burst"]}
     out["per_mode"] = per_mode
     # work stealing with 1..16 counter groups, contiguous ranges and striped ownership,
-    # interleaved rounds
+    # 1-second loops interleaved over 2 rounds
     wdescs = {f"{lay}_groups_{g}": pgt.make_desc(M, N, K, b_layout=pgt.B_KN, sched_mode=pgt.WORK_STEALING,
                                                  group_size=16, ws_groups=g, kernel_cfg=args.cfg, ws_layout=code)
               for lay, code in (("ranges", pgt.WS_RANGES), ("striped", pgt.WS_STRIPED)) for g in (1, 2, 4, 8, 16)}
     wsamples = {k: [] for k in wdescs}
-    for _ in range(4):
+    for _ in range(2):
         for k, d in wdescs.items():
-            _, per = time_launches(torch, lambda: ctx.gemm_ex(d, dA, dB, dC), 10, 2)
-            wsamples[k].extend(per)
+            wsamples[k].extend(time_sustained(torch, lambda: ctx.gemm_ex(d, dA, dB, dC), 1.0))
     out["work_stealing_groups"] = {k: {"tflops": FLOP / (float(np.median(v)) * 1e-3) / 1e12,
                                        "ms": float(np.median(v))} for k, v in wsamples.items()}
     # swizzle group width (column blocks per group), interleaved rounds
