@@ -74,6 +74,9 @@ def parse():
                     choices=["blocked", "interleaved", "swizzled", "work_stealing", "blocked_grouped_m",
                              "launch_control"], help="scheduler of the bf16 headline GEMM")
     ap.add_argument("--group", type=int, default=16, help="group_size of the bf16 headline GEMM")
+    ap.add_argument("--ws-groups", type=int, default=8, help="work-stealing counter groups of the bf16 headline GEMM")
+    ap.add_argument("--ws-layout", default="ranges", choices=["ranges", "striped"],
+                    help="work-stealing tile ownership of the bf16 headline GEMM")
     ap.add_argument("--no-ragged", action="store_true",
                     help="skip the ragged-tail GEMM set (timed per scheduler, with tail idle from traces)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
@@ -318,8 +321,9 @@ def run_ours(args, world, rank, local, pg):
 
     default_head = args.sched == "swizzled" and args.group == 16
     head = desc_for(pgt.SCHED[args.sched]) if default_head else pgt.make_desc(
-        M, N, K, b_layout=pgt.B_KN, sched_mode=pgt.SCHED[args.sched], group_size=args.group, ws_groups=8,
-        kernel_cfg=args.cfg)
+        M, N, K, b_layout=pgt.B_KN, sched_mode=pgt.SCHED[args.sched], group_size=args.group,
+        ws_groups=args.ws_groups, kernel_cfg=args.cfg,
+        ws_layout=pgt.WS_STRIPED if args.ws_layout == "striped" else pgt.WS_RANGES)
     if args.kernel == "add":
         return run_add_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peaks)
     if args.kernel == "mxfp8":
@@ -749,7 +753,10 @@ def main():
         FLOP = 2.0 * M * N * K
         WORKLOAD = WORKLOAD.replace("M=N=K=8192", f"M=N=K={args.size}")
     if args.sched != "swizzled" or args.group != 16:
-        WORKLOAD = WORKLOAD.replace("swizzled group_size=16", f"{args.sched} group_size={args.group}")
+        sched = args.sched
+        if sched == "work_stealing":
+            sched += f" ({args.ws_groups} counter groups, {args.ws_layout})"
+        WORKLOAD = WORKLOAD.replace("swizzled group_size=16", f"{sched} group_size={args.group}")
     world, rank, local, pg = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
