@@ -380,3 +380,58 @@ def test_launch_control_checker_rejects_planted_mistakes(plant):
         v[3].append(5)
     with pytest.raises(AssertionError):
         S.check_launch_control_trace(v, 6)
+
+
+# ------------------------------------------------- failure injection in the ticket model
+@pytest.mark.parametrize("layout", [S.WS_RANGES, S.WS_STRIPED])
+def test_ws_stale_counter_is_detected(layout):
+    # a counter left non-zero by an earlier launch (what the in-kernel reset and the host
+    # reset prevent) skips that group's first tickets: the log misses tiles
+    T, P, G = 120, 8, 4
+    st = S.WsState(T, P, G, layout)
+    st.counter[2] = 5
+    rnd = random.Random(11)
+    visits = [[] for _ in range(P)]
+    live = list(range(P))
+    while live:
+        c = rnd.choice(live)
+        t = st.fetch(c)
+        if t < 0:
+            live.remove(c)
+        else:
+            visits[c].append(t)
+    assert sum(len(v) for v in visits) == T - 5
+    with pytest.raises(AssertionError):
+        S.check_ws_trace(visits, T, G, layout)
+
+
+@pytest.mark.parametrize("layout", [S.WS_RANGES, S.WS_STRIPED])
+def test_ws_lost_ticket_is_detected(layout):
+    # a worker that takes a ticket and then stops without running the tile (an aborted
+    # worker) leaves a hole the validator reports
+    T, P, G = 90, 6, 3
+    rnd = random.Random(12)
+    visits = S.ws_simulate(T, P, G, lambda live: rnd.choice(live), layout=layout)
+    S.check_ws_trace(visits, T, G, layout)
+    c = max(range(P), key=lambda i: len(visits[i]))
+    visits[c].pop(len(visits[c]) // 2)
+    with pytest.raises(AssertionError):
+        S.check_ws_trace(visits, T, G, layout)
+
+
+def test_ws_counter_overflow_past_group_size_is_harmless():
+    # every exhausted group's counter ends above its size (the failing fetch still adds one);
+    # tickets beyond the size never become tiles
+    T, P, G = 50, 9, 4
+    rnd = random.Random(13)
+    st = S.WsState(T, P, G, S.WS_STRIPED)
+    live, seen = list(range(P)), []
+    while live:
+        c = rnd.choice(live)
+        t = st.fetch(c)
+        if t < 0:
+            live.remove(c)
+        else:
+            seen.append(t)
+    assert sorted(seen) == list(range(T))
+    assert all(st.counter[g] > len(st.tiles[g]) for g in range(G))
