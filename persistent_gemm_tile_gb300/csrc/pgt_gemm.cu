@@ -326,6 +326,16 @@ int gemm_launch(pgt_ctx* ctx, const pgt_gemm_desc& d, const pgt_gemm_plan_info& 
     gp.bias = (d.epilogue & PGT_EPI_BIAS) ? d.bias : nullptr;
     gp.C = static_cast<uint16_t*>(C);
     gp.ldc = d.ldc;
+    // K-direction period: the workers this configuration keeps resident at once (capped at
+    // T), whatever the scheduler or the requested worker count, so every scheduler gives a
+    // tile the same K order.  bf16 only (MXFP8 scales are loaded in forward K groups).
+    gp.kdir_period = 0;
+    if (!mx) {
+        KernelInfo k0;
+        rc = kernel_info(ctx->device, plan.kernel_cfg, mx, bmn, false, s, &k0);
+        if (rc) return rc;
+        gp.kdir_period = k0.max_workers < plan.tiles ? k0.max_workers : plan.tiles;
+    }
     gp.tr_visits = trace ? trace->visits : nullptr;
     gp.tr_max = trace ? trace->max_visits : 0;
     gp.tr_counts = trace ? trace->counts : nullptr;

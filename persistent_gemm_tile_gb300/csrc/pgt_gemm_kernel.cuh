@@ -43,6 +43,7 @@ struct GemmParams {
     const float* bias;  // fp32[N] or nullptr
     uint16_t* C;        // bf16 output (the last, narrower store chunk of a tile is written directly)
     int64_t ldc;        // elements
+    int kdir_period;    // bf16: tiles t with odd t / kdir_period run K backwards (0: all forward)
     int32_t* tr_visits;
     int64_t tr_max;
     int32_t* tr_counts;
@@ -287,7 +288,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int row0 = (m * CS + (int)rank) * L::BM;  // this CTA's rows of A
                 const int col0 = n * BN + (int)rank * L::BN_CTA;  // this CTA's slice of B
+                // K direction: tiles of alternate waves (t / kdir_period odd, the period being the
+                // number of workers the GPU holds at once) walk K backwards, so a wave starts on
+                // the K slices of the panels the previous wave read last, which are still in L2.
+                // The direction depends on the tile id alone: each tile's K order is fixed.
+                const bool rev = !MX && gp.kdir_period > 0 && ((t / gp.kdir_period) & 1) != 0;
                 for (int k = 0; k < gp.k_iters; ++k, ++it) {
+                    const int kc = rev ? gp.k_iters - 1 - k : k;  // K slice loaded at iteration k
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
                     if (!mbar_wait(empty(s), ph ^ 1u, abort_flag, gp.err, kRoleProducer, 1)) {
@@ -299,13 +306,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const bool sf_now = MX && (k & 3) == 0;
                     if (leader) mbar_arrive_expect_tx(full(s), CS * (L::TX_BYTES + (sf_now ? L::SF_TX_BYTES : 0)));
                     const uint32_t fb = kPair ? mapa_shared(full(s), 0) : full(s);
-                    tma_load<CS>(sa, &tmA, fb, k * L::BK, row0);
+                    tma_load<CS>(sa, &tmA, fb, kc * L::BK, row0);
                     if constexpr (B_MN) {
 #pragma unroll
                         for (int j = 0; j < L::BN_CTA / 64; ++j)
-                            tma_load<CS>(sb + j * 8192, &tmB, fb, col0 + 64 * j, k * L::BK);
+                            tma_load<CS>(sb + j * 8192, &tmB, fb, col0 + 64 * j, kc * L::BK);
                     } else {
-                        tma_load<CS>(sb, &tmB, fb, k * L::BK, col0);
+                        tma_load<CS>(sb, &tmB, fb, kc * L::BK, col0);
                     }
                     if constexpr (MX) {
                         if (sf_now) {
