@@ -288,11 +288,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int row0 = (m * CS + (int)rank) * L::BM;  // this CTA's rows of A
                 const int col0 = n * BN + (int)rank * L::BN_CTA;  // this CTA's slice of B
-                // K direction: tiles of alternate waves (t / kdir_period odd, the period being the
-                // number of workers the GPU holds at once) walk K backwards, so a wave starts on
-                // the K slices of the panels the previous wave read last, which are still in L2.
-                // The direction depends on the tile id alone: each tile's K order is fixed.
-                const bool rev = !MX && gp.kdir_period > 0 && ((t / gp.kdir_period) & 1) != 0;
+                // K direction: tiles of alternate waves walk K backwards, so a wave starts on the
+                // K slices of the panels the previous wave read last, which are still in L2.
+                // A tile's wave is its position in the 16-column-group order (the swizzled
+                // order with group 16) divided by kdir_period, the number of workers the GPU
+                // holds at once.  It depends on (m, n) alone, so each output tile has one K
+                // order whatever the scheduler, group size or worker count.
+                bool rev = false;
+                if (!MX && gp.kdir_period > 0) {
+                    const int g16 = min(16, gp.sp.n_tiles);
+                    const int grp = n / g16;
+                    const int gw = min(g16, gp.sp.n_tiles - grp * g16);
+                    const int pos = grp * g16 * gp.sp.m_tiles + m * gw + (n - grp * g16);
+                    rev = ((pos / gp.kdir_period) & 1) != 0;
+                }
                 for (int k = 0; k < gp.k_iters; ++k, ++it) {
                     const int kc = rev ? gp.k_iters - 1 - k : k;  // K slice loaded at iteration k
                     const int s = it % STAGES;
