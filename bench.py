@@ -41,9 +41,9 @@ L2_NOTE = "inputs larger than L2: A+B+C = 384 MiB per GEMM > 129 MB L2; add x+y+
 GEMM_SOURCES = ["csrc/pgt_gemm_kernel.cuh", "csrc/pgt_device.cuh", "csrc/pgt_sched.cuh"]
 ADD_SOURCES = ["csrc/pgt_add.cu", "csrc/pgt_device.cuh", "csrc/pgt_sched.cuh"]
 PROFILED_TRAFFIC = {
-    "gemm_bf16_2cta_256x256": (1.197656e+09 + 1.281603e+08, GEMM_SOURCES, "c6efaff8e95d97c6"),
-    "gemm_mxfp8_2cta_256x256": (2.543516e+08 + 1.166008e+08, GEMM_SOURCES, "c6efaff8e95d97c6"),
-    "add_wide_8x1024": (5.369321e+08 + 2.292219e+08, ADD_SOURCES, "ba6a4f5c86e81ce0"),
+    "gemm_bf16_2cta_256x256": (9.161178e+08 + 1.285768e+08, GEMM_SOURCES, "95e9e8c757920309"),
+    "gemm_mxfp8_2cta_256x256": (2.483269e+08 + 1.173100e+08, GEMM_SOURCES, "95e9e8c757920309"),
+    "add_wide_8x1024": (5.369303e+08 + 2.296192e+08, ADD_SOURCES, "ba6a4f5c86e81ce0"),
 }
 
 
