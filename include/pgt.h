@@ -247,8 +247,10 @@ int pgt_gemm_plan(const pgt_ctx* ctx, const pgt_gemm_desc* desc, pgt_gemm_plan_i
  *   trace: NULL, or buffers for a traced launch (a slower kernel variant that records
  *        every visit; used to check the schedule and the tail idle time).
  * Every output element is reduced over K in the same order whatever the scheduler, so for
- * one kernel_cfg the result is bit-identical across sched_mode, group_size, ws_groups
- * and num_workers.  Work stealing uses the context's counters: one work-stealing launch
+ * one kernel_cfg the result is bit-identical across sched_mode, group_size, ws_groups,
+ * ws_layout and num_workers.  (bf16 tiles of alternate waves walk K backwards.  A tile's
+ * direction follows from its position and from how many workers the GPU holds at once,
+ * so results can differ in the last bit between GPUs with different SM counts.)  Work stealing uses the context's counters: one work-stealing launch
  * per context may be in flight at a time. */
 int pgt_gemm_ex(pgt_ctx* ctx, const pgt_gemm_desc* desc, const void* A, const void* B,
                 const uint8_t* sfa, const uint8_t* sfb, void* C, void* workspace,
