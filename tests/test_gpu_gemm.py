@@ -10,7 +10,7 @@ import torch
 
 import persistent_gemm_tile_gb300 as pgt
 import synthetic
-from gpu_helpers import dev_u16, host_u16, need_gpu, sample_rows
+from gpu_helpers import dev_u16, host_u16, need_gpu
 from oracle import gemm as OG
 from oracle import numerics as NM
 from oracle import schedule as S
@@ -30,9 +30,9 @@ def ctx():
 
 
 def run(ctx, A, B, M, N, K, *, b_layout=pgt.B_KN, mode=pgt.SWIZZLED, G=16, cfg=pgt.CFG_AUTO, lda=0, ldb=0,
-        ldc=0, ws_groups=0, workers=0, trace=False):
+        ldc=0, ws_groups=0, workers=0, trace=False, ws_layout=pgt.WS_RANGES):
     desc = pgt.make_desc(M, N, K, lda=lda, ldb=ldb, ldc=ldc, b_layout=b_layout, sched_mode=mode, group_size=G,
-                         ws_groups=ws_groups, kernel_cfg=cfg, num_workers=workers)
+                         ws_groups=ws_groups, kernel_cfg=cfg, num_workers=workers, ws_layout=ws_layout)
     plan = ctx.gemm_plan(desc)
     C = torch.full((M, ldc or N), -1, dtype=torch.int16, device="cuda")
     tb = pgt.TraceBuffers(plan["ctas"], plan["tiles"]) if trace else None
@@ -91,23 +91,20 @@ def test_256_all_modes_schedule_and_values(ctx):
         C, plan, tb = run(ctx, dev_u16(A), dev_u16(B), M, N, K, mode=mode, G=G, cfg=pgt.CFG_1CTA_128x128,
                           trace=True)
         assert plan["tiles"] == 4 and plan["workers"] == 4
+        assert plan["ws_groups"] == 4  # eight requested, one per worker in use
         c = host_u16(C)
         OG.check(c, C64, Abs)
         outs.append(c)
         visits, _ = tb.read()
         grid = S.Grid(plan["m_blocks"], plan["n_blocks"], 1)
         if mode == pgt.WORK_STEALING:
-            S.check_ws_trace([[t for (t, _, _, _) in v] for v in visits], grid.tiles, plan_ws(ctx))
+            S.check_ws_trace([[t for (t, _, _, _) in v] for v in visits], grid.tiles, plan["ws_groups"])
         else:
             want = S.static_schedule(mode, grid, plan["workers"], G)
             assert [[(t, m, n) for (t, m, n, _) in v] for v in visits] == \
                    [[(t, m, n) for (_, t, m, n) in v] for v in want]
     for c in outs[1:]:
         assert np.array_equal(c, outs[0])
-
-
-def plan_ws(ctx):
-    return min(8, ctx.max_groups)
 
 
 def worker_visits(visits, cs):
@@ -170,7 +167,7 @@ def test_modes_bit_identical_with_traces(ctx, cfg, workers):
             visits = worker_visits(visits, cs)
             grid = S.Grid(plan["m_blocks"], plan["n_blocks"], cs)
             if mode == pgt.WORK_STEALING:
-                S.check_ws_trace([[t for (t, _, _, _) in v] for v in visits], grid.tiles, 4)
+                S.check_ws_trace([[t for (t, _, _, _) in v] for v in visits], grid.tiles, plan["ws_groups"])
             else:
                 want = S.static_schedule(mode, grid, plan["workers"], G)
                 assert [[(t, m, n) for (t, m, n, _) in v] for v in visits] == \
@@ -186,21 +183,35 @@ def ragged_inputs():
     return synthetic.gemm_bf16_sequence(RAGGED, seed=3, dist="uniform")
 
 
-@pytest.mark.parametrize("cfg", [pgt.CFG_1CTA_128x256, pgt.CFG_2CTA_256x128])
+@pytest.fixture(scope="module")
+def ragged_oracle(ragged_inputs):
+    """fp64 C and |A|.|B| of each ragged shape, computed once per module."""
+    cache = {}
+
+    def get(idx):
+        if idx not in cache:
+            M, N, K = RAGGED[idx]
+            A, B = ragged_inputs[idx]
+            cache[idx] = oracle_full(A, B, M, N, K)
+        return cache[idx]
+    return get
+
+
+@pytest.mark.parametrize("cfg", [pgt.CFG_AUTO, pgt.CFG_1CTA_128x256, pgt.CFG_2CTA_256x128])
 @pytest.mark.parametrize("idx", [0, 1, 2])
-def test_ragged_set_all_modes(ctx, ragged_inputs, idx, cfg):
+def test_ragged_set_all_modes(ctx, ragged_inputs, ragged_oracle, idx, cfg):
+    """Every element of C against the fp64 oracle (first mode), then bit identity across
+    the other schedulers."""
     M, N, K = RAGGED[idx]
     A, B = ragged_inputs[idx]
     dA, dB = dev_u16(A), dev_u16(B)
     ref = None
-    for mode in ALL_MODES:
+    for mode in ALL_MODES + [pgt.LAUNCH_CONTROL]:
         C, plan, _ = run(ctx, dA, dB, M, N, K, mode=mode, G=16, cfg=cfg)
         if ref is None:
             ref = C
-            rows = sample_rows(M, plan["bm"], 24, seed=idx)
-            A64, B64 = OG.dequant_bf16(A), OG.dequant_bf16(B)
-            C64, Abs = OG.gemm_rows(A64, B64, True, K, N, rows)
-            OG.check(host_u16(C)[rows], C64, Abs)
+            C64, Abs = ragged_oracle(idx)
+            OG.check(host_u16(C), C64, Abs)
         else:
             assert torch.equal(C, ref), mode
 
@@ -213,17 +224,70 @@ def big_inputs():
     return A, B
 
 
-@pytest.mark.parametrize("cfg", [pgt.CFG_AUTO, pgt.CFG_2CTA_256x128, pgt.CFG_2CTA_256x256])
-def test_8192_swizzled_vs_work_stealing(ctx, big_inputs, cfg):
+@pytest.fixture(scope="module")
+def big_oracle(big_inputs):
+    A, B = big_inputs
+    return oracle_full(A, B, 8192, 8192, 8192)
+
+
+@pytest.mark.parametrize("cfg", [pgt.CFG_AUTO, pgt.CFG_1CTA_128x128, pgt.CFG_1CTA_128x256, pgt.CFG_2CTA_256x128])
+def test_8192_full_matrix_swizzled_vs_work_stealing(ctx, big_inputs, big_oracle, cfg):
+    """The benchmark workload: all 8192 x 8192 outputs against the fp64 oracle, and work
+    stealing (both tile ownerships) and launch control bit-identical to the swizzled order.
+    AUTO must keep the pair 256 x 256 tile at this size."""
     M = N = K = 8192
     A, B = big_inputs
     dA, dB = dev_u16(A), dev_u16(B)
     C1, plan, _ = run(ctx, dA, dB, M, N, K, mode=pgt.SWIZZLED, G=16, cfg=cfg)
-    C2, _, _ = run(ctx, dA, dB, M, N, K, mode=pgt.WORK_STEALING, G=16, cfg=cfg)
-    assert torch.equal(C1, C2)
-    rows = sample_rows(M, plan["bm"], 26, seed=2)
-    C64, Abs = OG.gemm_rows(OG.dequant_bf16(A), OG.dequant_bf16(B), True, K, N, rows)
-    OG.check(host_u16(C1)[rows], C64, Abs)
+    if cfg == pgt.CFG_AUTO:
+        assert plan["kernel_cfg"] == pgt.CFG_2CTA_256x256
+    C64, Abs = big_oracle
+    OG.check(host_u16(C1), C64, Abs)
+    for kw in (dict(mode=pgt.WORK_STEALING), dict(mode=pgt.WORK_STEALING, ws_layout=pgt.WS_STRIPED),
+               dict(mode=pgt.LAUNCH_CONTROL)):
+        C2, _, _ = run(ctx, dA, dB, M, N, K, G=16, cfg=cfg, **kw)
+        assert torch.equal(C1, C2), kw
+
+
+# ------------------------------------------------------------------ AUTO per shape
+@pytest.mark.parametrize("M,N,K,b_layout", [(256, 256, 256, pgt.B_KN), (128, 16384, 16384, pgt.B_KN),
+                                            (8192, 8192, 8192, pgt.B_KN), (3000, 5000, 1024, pgt.B_NK),
+                                            (1, 8, 8, pgt.B_KN)])
+def test_auto_picks_a_candidate_whatever_the_scheduler(ctx, M, N, K, b_layout):
+    """AUTO resolves to one of its candidate tiles, and to the same one for every scheduler
+    and worker count (the choice depends on the problem alone)."""
+    cfgs = set()
+    for mode in ALL_MODES + [pgt.LAUNCH_CONTROL]:
+        for workers in (0, 1):
+            if mode == pgt.LAUNCH_CONTROL and workers:
+                continue
+            d = pgt.make_desc(M, N, K, b_layout=b_layout, sched_mode=mode, num_workers=workers)
+            cfgs.add(ctx.gemm_plan(d)["kernel_cfg"])
+    assert len(cfgs) == 1
+    assert cfgs.pop() in (pgt.CFG_1CTA_128x128, pgt.CFG_1CTA_128x256, pgt.CFG_2CTA_256x256)
+
+
+# ------------------------------------------------------------- the flat form
+def test_flat_gemm_ws_groups(ctx):
+    """pgt_gemm's counter-group count: work stealing on 1, 3 and 16 groups gives the bits of
+    the swizzled order; a count above the context's max_groups is rejected."""
+    M, N, K = 1000, 1104, 320
+    A, B = synthetic.gemm_bf16_inputs(M, N, K, seed=16)
+    dA, dB = dev_u16(A), dev_u16(B)
+    ref = torch.full((M, N), -1, dtype=torch.int16, device="cuda")
+    ctx.gemm(dA, dB, ref, M, N, K, sched_mode=pgt.SWIZZLED)
+    torch.cuda.synchronize()
+    C64, Abs = oracle_full(A, B, M, N, K)
+    OG.check(host_u16(ref), C64, Abs)
+    for g in (1, 3, 16, 0):
+        C = torch.full((M, N), -1, dtype=torch.int16, device="cuda")
+        ctx.gemm(dA, dB, C, M, N, K, sched_mode=pgt.WORK_STEALING, ws_groups=g)
+        torch.cuda.synchronize()
+        assert ctx.last_error()[0] == 0
+        assert torch.equal(C, ref), g
+    with pytest.raises(pgt.PgtError) as e:
+        ctx.gemm(dA, dB, ref, M, N, K, sched_mode=pgt.WORK_STEALING, ws_groups=ctx.max_groups + 1)
+    assert e.value.status == pgt.ERR_GROUPS
 
 
 # ------------------------------------------------------------------- errors

@@ -12,7 +12,7 @@ import torch
 
 import persistent_gemm_tile_gb300 as pgt
 import synthetic
-from gpu_helpers import dev_u8, host_u16, need_gpu, sample_rows
+from gpu_helpers import dev_u8, host_u16, need_gpu
 from oracle import gemm as OG
 from oracle import numerics as NM
 from oracle import schedule as S
@@ -102,7 +102,7 @@ def test_random_modes_bit_identical_with_traces(ctx, cfg):
         wv = [visits[w * cs] for w in range(plan["workers"])]
         grid = S.Grid(plan["m_blocks"], plan["n_blocks"], cs)
         if mode == pgt.WORK_STEALING:
-            S.check_ws_trace([[t for (t, _, _, _) in v] for v in wv], grid.tiles, min(8, ctx.max_groups))
+            S.check_ws_trace([[t for (t, _, _, _) in v] for v in wv], grid.tiles, plan["ws_groups"])
         else:
             want = S.static_schedule(mode, grid, plan["workers"], 3)
             assert [[(t, m, n) for (t, m, n, _) in v] for v in wv] == [[(t, m, n) for (_, t, m, n) in v] for v in want]
@@ -139,19 +139,36 @@ def big_mx():
     return synthetic.gemm_mxfp8_inputs(M, N, K, seed=4)
 
 
+@pytest.fixture(scope="module")
+def big_mx_oracle(big_mx):
+    qa, sa, qb, sb = big_mx
+    return OG.gemm_full(OG.dequant_mxfp8(qa, sa), OG.dequant_mxfp8(qb, sb), False, 8192, 8192, 8192)
+
+
 @pytest.mark.parametrize("cfg", [pgt.CFG_AUTO, pgt.CFG_1CTA_128x256, pgt.CFG_2CTA_256x224])
-def test_8192_mxfp8_swizzled_sampled_rows(ctx, big_mx, cfg):
+def test_8192_mxfp8_full_matrix(ctx, big_mx, big_mx_oracle, cfg):
+    """The MXFP8 benchmark workload: every output against the fp64 oracle, and work
+    stealing bit-identical to the swizzled order."""
     M = N = K = 8192
     qa, sa, qb, sb = big_mx
     d = dev(qa, sa, qb, sb)
     C, plan, _ = run_mx(ctx, *d, M, N, K, cfg=cfg, mode=pgt.SWIZZLED, G=16)
+    C64, Abs = big_mx_oracle
+    OG.check(host_u16(C), C64, Abs)
     C2, _, _ = run_mx(ctx, *d, M, N, K, cfg=cfg, mode=pgt.WORK_STEALING, G=16)
     assert torch.equal(C, C2)
-    rows = sample_rows(M, 128 * plan["cluster_size"], 22, seed=4)
-    A64 = OG.dequant_mxfp8(qa[rows], sa[rows])
-    B64 = OG.dequant_mxfp8(qb, sb)
-    C64, Abs = OG.gemm_rows(A64, B64, False, K, N, np.arange(rows.size))
-    OG.check(host_u16(C)[rows], C64, Abs)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (128, 16384, 1024), (2048, 2048, 2048), (8192, 8192, 8192),
+                                   (3000, 5000, 1024)])
+def test_auto_configuration_and_workspace_agree(ctx, M, N, K):
+    """AUTO picks per shape among the 128-multiple tiles, whose packed-scale layout is the
+    same, so the workspace size (queried without a context) fits whatever AUTO picks."""
+    auto = pgt.make_desc(M, N, K, dtype=pgt.MXFP8, b_layout=pgt.B_NK)
+    plan = ctx.gemm_plan(auto)
+    assert plan["kernel_cfg"] in (pgt.CFG_1CTA_128x128, pgt.CFG_1CTA_128x256, pgt.CFG_2CTA_256x256)
+    fixed = pgt.make_desc(M, N, K, dtype=pgt.MXFP8, b_layout=pgt.B_NK, kernel_cfg=plan["kernel_cfg"])
+    assert ctx.gemm_workspace_bytes(auto) == ctx.gemm_workspace_bytes(fixed)
 
 
 def test_mxfp8_argument_errors(ctx):
