@@ -67,11 +67,15 @@ extern "C" {
  *   INTERLEAVED:       worker p visits p, p+P, p+2P, ... with the linear decode ([PK]).
  *   SWIZZLED:          interleaved waves (tile = P*w + p, [TS]) with the group_size
  *                      column-group decode and 2-CTA pairing ([TS]).
- *   WORK_STEALING:     tiles handed out through per-group atomic counters; ws_groups
- *                      counters, group g owns tiles [g*T/G, (g+1)*T/G) (or, with
- *                      PGT_WS_STRIPED, the tiles t = g mod G); a worker starts at group
- *                      (p mod G) and steals from the following groups ([WS]); tiles
- *                      decoded like SWIZZLED (linear when group_size == 1).
+ *   WORK_STEALING:     tiles handed out through per-group atomic counters; G counters,
+ *                      group g owns tiles [g*T/G, (g+1)*T/G) (or, with PGT_WS_STRIPED,
+ *                      the tiles t = g mod G); a worker starts at group (p mod G) and
+ *                      steals from the following groups ([WS]); tiles decoded like
+ *                      SWIZZLED (linear when group_size == 1).  G = min(ws_groups, P):
+ *                      every group has a home worker, as on the page, where the groups
+ *                      (XCDs) are far fewer than the workers (CUs).  A worker takes its
+ *                      home group's next ticket a few pipeline stages before it needs it;
+ *                      the release flag is read before each ticket is taken.
  *   BLOCKED_GROUPED_M: blocked order with the L2-grouping decode, bands of group_size
  *                      tile rows ([PK] "PERSISTENT BLOCKED WITH L2 GROUPING").
  * P is the number of persistent workers (CTAs, or CTA pairs for 2-CTA kernels) and
@@ -165,6 +169,7 @@ typedef struct pgt_gemm_plan_info {
     int32_t ctas;            /* P * cluster_size */
     int32_t k_iters;         /* ceil(K / bk) */
     int32_t smem_bytes;      /* dynamic shared memory per CTA */
+    int32_t ws_groups;       /* work-stealing counter groups in use: min(ws_groups, workers) */
 } pgt_gemm_plan_info;
 
 /* Optional launch trace (all DEVICE pointers, caller-owned).
@@ -250,18 +255,22 @@ int pgt_gemm_plan(const pgt_ctx* ctx, const pgt_gemm_desc* desc, pgt_gemm_plan_i
  * one kernel_cfg the result is bit-identical across sched_mode, group_size, ws_groups,
  * ws_layout and num_workers.  (bf16 tiles of alternate waves walk K backwards.  A tile's
  * direction follows from its position and from how many workers the GPU holds at once,
- * so results can differ in the last bit between GPUs with different SM counts.)  Work stealing uses the context's counters: one work-stealing launch
- * per context may be in flight at a time. */
+ * so results can differ in the last bit between GPUs with different SM counts.)  Work
+ * stealing uses the context's counters: one work-stealing launch per context may be in
+ * flight at a time. */
 int pgt_gemm_ex(pgt_ctx* ctx, const pgt_gemm_desc* desc, const void* A, const void* B,
                 const uint8_t* sfa, const uint8_t* sfb, void* C, void* workspace,
                 size_t workspace_bytes, const pgt_trace* trace, void* stream);
 
-/* The flat form of the entry point ([WS] matmul(a, b, c, ..., work_stealing)):
- * packed leading dimensions, PGT_CFG_AUTO, ws_groups = min(8, max_groups), one worker
- * per SM (pair).  Arguments as in pgt_gemm_ex. */
+/* The flat form of the entry point ([WS] matmul(a, b, c, ..., work_stealing), with the
+ * counter-group count of MatmulConfig): packed leading dimensions, PGT_CFG_AUTO, one worker
+ * per SM (pair), contiguous counter ranges.  ws_groups: work-stealing counter groups,
+ * 1 .. max_groups of the context, 0 = min(8, max_groups); a value outside [0, 64] returns
+ * PGT_ERR_GROUPS before anything else is checked, one above the context's max_groups
+ * returns PGT_ERR_GROUPS too.  Other arguments as in pgt_gemm_ex. */
 int pgt_gemm(pgt_ctx* ctx, const void* A, const void* B, const uint8_t* sfa,
              const uint8_t* sfb, void* C, int64_t M, int64_t N, int64_t K, int dtype,
-             int b_layout, int sched_mode, int group_size, void* workspace,
+             int b_layout, int sched_mode, int group_size, int ws_groups, void* workspace,
              size_t workspace_bytes, void* stream);
 
 /* End-to-end GEMM from host memory: copies h_A, h_B (and h_sfa, h_sfb for MXFP8) into the
@@ -322,7 +331,8 @@ int pgt_multi_loop(pgt_ctx* ctx, const pgt_scale_space* spaces, int n_spaces, in
  * each worker's visits in `trace` (one record list per WORKER, not per CTA).  One
  * single-thread worker per block; num_workers >= 1, and for PGT_LAUNCH_CONTROL exactly the
  * tile count (one worker per tile; cancelled workers record nothing).  Work stealing uses
- * the context's counters and release flags like the GEMM, with ws_layout a PGT_WS_*. */
+ * the context's counters and release flags like the GEMM, with ws_layout a PGT_WS_* and
+ * min(ws_groups, num_workers) counter groups. */
 int pgt_schedule_log(pgt_ctx* ctx, int64_t m_blocks, int64_t n_blocks, int cluster_size,
                      int sched_mode, int group_size, int ws_groups, int ws_layout, int num_workers,
                      const pgt_trace* trace, void* stream);
@@ -341,9 +351,13 @@ int pgt_schedule_log(pgt_ctx* ctx, int64_t m_blocks, int64_t n_blocks, int clust
  *   A, B, C, M, N, K, b_layout, group_size: as in pgt_gemm (bf16 only).
  *   ws_groups: 1 .. PGT_NOALLOC_MAX_GROUPS (0 = 8); larger values return PGT_ERR_GROUPS.
  *   d_err: NULL, or a caller-owned DEVICE int32[4] the kernel writes if a bounded wait
- *          runs out (code, role, block, site); this call does not clear it.
+ *          runs out (code, role, block, site); this call does not clear it.  With NULL a
+ *          timeout only lands in a line of the shared array, which the next call clears and
+ *          no call reads: the call still returns PGT_OK and C may be incomplete.  Callers
+ *          that must detect a timeout pass d_err and read it after the stream finishes.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- * with that device current; make that first call before any stream capture.  Every call
+ * with that device current; make that first call before any stream capture.  A first
+ * call made while `stream` is capturing returns PGT_ERR_ARG and enqueues nothing.  Every call
  * clears the counters on `stream` before its launch.  All calls share the one array per
  * device: calls that overlap on the GPU (different streams, or graph replays running
  * concurrently) race on it and give wrong results. */

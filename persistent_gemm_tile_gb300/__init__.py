@@ -54,7 +54,7 @@ class GemmDesc(ctypes.Structure):
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "kernel_cfg", "bm", "bn", "bk", "cluster_size", "stages", "m_blocks", "n_blocks", "m_tiles",
-        "tiles", "workers", "ctas", "k_iters", "smem_bytes")]
+        "tiles", "workers", "ctas", "k_iters", "smem_bytes", "ws_groups")]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -99,7 +99,7 @@ def lib() -> ctypes.CDLL:
         L.pgt_gemm_workspace_bytes.restype = SZ
         L.pgt_gemm_plan.argtypes = [P, P, P]
         L.pgt_gemm_ex.argtypes = [P, P, P, P, P, P, P, P, SZ, P, P]
-        L.pgt_gemm.argtypes = [P, P, P, P, P, P, I64, I64, I64, I, I, I, I, P, SZ, P]
+        L.pgt_gemm.argtypes = [P, P, P, P, P, P, I64, I64, I64, I, I, I, I, I, P, SZ, P]
         L.pgt_gemm_host.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
         L.pgt_add.argtypes = [P, P, P, P, I64, I64, I64, I64, I64, I, I, I, I, P, P]
         L.pgt_add_workers.argtypes = [P, I64, I64, I, I, I]
@@ -224,14 +224,15 @@ class Context:
                                  _ptr(workspace), workspace_bytes, ctypes.byref(trace) if trace else None,
                                  _stream(stream)), "pgt_gemm_ex")
 
-    def gemm(self, A, B, C, M, N, K, dtype=BF16, b_layout=B_KN, sched_mode=SWIZZLED, group_size=16, sfa=None,
-             sfb=None, workspace=None, workspace_bytes=0, stream=None) -> None:
+    def gemm(self, A, B, C, M, N, K, dtype=BF16, b_layout=B_KN, sched_mode=SWIZZLED, group_size=16, ws_groups=0,
+             sfa=None, sfb=None, workspace=None, workspace_bytes=0, stream=None) -> None:
+        """pgt_gemm, the flat form: packed operands, automatic kernel configuration."""
         if isinstance(sched_mode, str):
             sched_mode = SCHED[sched_mode]
         if workspace is not None and not workspace_bytes:
             workspace_bytes = workspace.numel() * workspace.element_size()
         _check(lib().pgt_gemm(self.handle, _ptr(A), _ptr(B), _ptr(sfa), _ptr(sfb), _ptr(C), M, N, K, dtype,
-                              b_layout, sched_mode, group_size, _ptr(workspace), workspace_bytes,
+                              b_layout, sched_mode, group_size, ws_groups, _ptr(workspace), workspace_bytes,
                               _stream(stream)), "pgt_gemm")
 
     def gemm_host(self, desc: GemmDesc, hA, hB, hC, dA, dB, dC, h_sfa=None, h_sfb=None, d_sfa=None, d_sfb=None,

@@ -106,7 +106,7 @@ int schedule_log_launch(pgt_ctx* ctx, int64_t m_blocks, int64_t n_blocks, int cl
         g = sp.n_tiles;
     }
     sp.group = g;
-    sp.ws_groups = ws_groups;
+    sp.ws_groups = ws_groups < num_workers ? ws_groups : num_workers;  // every group has a home worker
     sp.ws_layout = ws_layout;
     sp.workers = num_workers;
     sp.counters = ctx->d_counters;
@@ -256,10 +256,12 @@ int pgt_gemm_ex(pgt_ctx* ctx, const pgt_gemm_desc* desc, const void* A, const vo
 }
 
 int pgt_gemm(pgt_ctx* ctx, const void* A, const void* B, const uint8_t* sfa, const uint8_t* sfb, void* C, int64_t M,
-             int64_t N, int64_t K, int dtype, int b_layout, int sched_mode, int group_size, void* workspace,
-             size_t workspace_bytes, void* stream) {
+             int64_t N, int64_t K, int dtype, int b_layout, int sched_mode, int group_size, int ws_groups,
+             void* workspace, size_t workspace_bytes, void* stream) {
+    if (ws_groups < 0 || ws_groups > kMaxGroups) return PGT_ERR_GROUPS;  // no context can hold that many
     pgt_gemm_desc d;
     memset(&d, 0, sizeof(d));
+    d.ws_groups = ws_groups;
     d.M = M;
     d.N = N;
     d.K = K;

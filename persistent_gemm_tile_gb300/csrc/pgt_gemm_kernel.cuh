@@ -55,6 +55,8 @@ constexpr int kTileRing = 4;            // tile-id ring depth
 constexpr int kEpiWarps = 4;
 constexpr int kEpiBufBytes = 32 * 128;  // 32 rows x 64 bf16, 128B-swizzled, per buffer
 constexpr int kMaxSmem = 232448;        // 227 KB dynamic shared memory per CTA
+constexpr int kTicketLead = 4;          // work stealing: stages before a tile's last load that the
+                                        // next ticket is taken
 
 constexpr int pow2_at_least(int v) {
     int p = 32;
@@ -164,6 +166,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = rank == 0;
     const int worker = blockIdx.x / CS;
 
+    // The producer thread of the worker (the leader CTA's thread 0) runs the scheduler.
+    // Work stealing takes the first ticket here, so its round trip overlaps the set-up below.
+    Scheduler sch;
+    if (threadIdx.x == 0 && leader) {
+        sch.init(gp.sp, worker);
+        sch.take_ahead();
+    }
+
     const uint32_t bar0 = base + L::BAR_OFF;
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -221,9 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 prefetch_tensormap(&tmSFA);
                 prefetch_tensormap(&tmSFB);
             }
-            Scheduler sch;
-            if (leader) sch.init(gp.sp, worker);
             const bool clc = gp.sp.mode == kLaunchControl;
+            const int lead_k = gp.k_iters > kTicketLead ? gp.k_iters - kTicketLead : 0;
             bool clc_first = true, clc_pending = false;
             uint32_t clc_phase = 0;
             // launch control: the worker's own tile first, then tiles of clusters it cancels
@@ -330,6 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load<CS>(sa + L::SFB_OFF, &tmSFB, fb, 0, kg * gp.sfb_rows + n * L::NB128);
                         }
                     }
+                    // work stealing: the next tile's ticket, kTicketLead stages early (its value
+                    // is first read by the next fetch)
+                    if (leader && k == lead_k) sch.take_ahead();
                 }
             }
             if (leader) sch.finish();
@@ -480,32 +492,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (L::ACC_BUFS == 1) {
                 // a single accumulator: read all of it into registers (as bf16 pairs), hand
                 // it back to the MMA warp at once, then stage and store
+                // pk[j] holds columns 2j and 2j + 1; the accumulator is read 128 columns per
+                // wait, so the MMA warp gets it back after two load round trips
+                static_assert(BN % 128 == 0, "single-accumulator tiles are read 128 columns at a time");
                 uint32_t pk[BN / 2];
                 if (!gp.epi) {
 #pragma unroll
-                    for (int c = 0; c < BN / 64; ++c) {
-                        uint32_t r0[32], r1[32];
-                        tmem_ld_32x32b_x32(tacc + c * 64, r0);
-                        tmem_ld_32x32b_x32(tacc + c * 64 + 32, r1);
+                    for (int h = 0; h < BN / 128; ++h) {
+                        uint32_t r[4][32];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) tmem_ld_32x32b_x32(tacc + h * 128 + 32 * q, r[q]);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            pk[32 * c + i] = pack_bf16x2(r0[2 * i], r0[2 * i + 1]);
-                            pk[32 * c + 16 + i] = pack_bf16x2(r1[2 * i], r1[2 * i + 1]);
-                        }
+                        for (int q = 0; q < 4; ++q)
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) pk[64 * h + 16 * q + i] = pack_bf16x2(r[q][2 * i], r[q][2 * i + 1]);
                     }
                 } else {
 #pragma unroll
-                    for (int c = 0; c < BN / 64; ++c) {
-                        uint32_t r0[32], r1[32];
-                        tmem_ld_32x32b_x32(tacc + c * 64, r0);
-                        tmem_ld_32x32b_x32(tacc + c * 64 + 32, r1);
+                    for (int h = 0; h < BN / 128; ++h) {
+                        uint32_t r[4][32];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) tmem_ld_32x32b_x32(tacc + h * 128 + 32 * q, r[q]);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            pk[32 * c + i] = cvt(r0[2 * i], r0[2 * i + 1], col0 + 64 * c + 2 * i);
-                            pk[32 * c + 16 + i] = cvt(r1[2 * i], r1[2 * i + 1], col0 + 64 * c + 32 + 2 * i);
-                        }
+                        for (int q = 0; q < 4; ++q)
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                pk[64 * h + 16 * q + i] =
+                                    cvt(r[q][2 * i], r[q][2 * i + 1], col0 + 128 * h + 32 * q + 2 * i);
                     }
                 }
                 tc_fence_before();
@@ -556,6 +571,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     auto tv = [&](int i) __attribute__((always_inline)) -> uint32_t {
                         if constexpr (kTail == 16)
                             return tb[i];
+                        else if constexpr (kTail == 32)
+                            return ta[i];
                         else
                             return i < 32 ? ta[i] : tb[i - 32];
                     };

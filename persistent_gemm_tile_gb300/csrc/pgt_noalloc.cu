@@ -33,11 +33,14 @@ std::mutex g_mutex;
 
 // Once per device, with that device current: resolve the array's device address (the
 // host-side symbol is only a stand-in and must never be handed to a kernel) and the SM
-// count.
-int device_setup(int device, DeviceScratch* out) {
+// count.  The lookup may load the module, so it is refused while `stream` is capturing.
+int device_setup(int device, cudaStream_t stream, DeviceScratch* out) {
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceScratch& s = g_devices[device];
     if (!s.ready) {
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return PGT_ERR_CUDA;
+        if (cap != cudaStreamCaptureStatusNone) return PGT_ERR_ARG;
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return PGT_ERR_CUDA;
         int sms = 0;
@@ -61,8 +64,9 @@ extern "C" int pgt_gemm_noalloc(const void* A, const void* B, void* C, int64_t M
     int device = -1;
     if (cudaGetDevice(&device) != cudaSuccess) return PGT_ERR_CUDA;
     if (device < 0 || device >= kNoallocMaxDevices) return PGT_ERR_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
     DeviceScratch ds;
-    int rc = device_setup(device, &ds);
+    int rc = device_setup(device, st, &ds);
     if (rc) return rc;
 
     // a context that only points into the static scratch; nothing here is allocated
@@ -73,6 +77,8 @@ extern "C" int pgt_gemm_noalloc(const void* A, const void* B, void* C, int64_t M
     c.flags = 0;
     c.d_counters = ds.scratch;
     c.d_done = ds.scratch + pgt::kCounterStride * PGT_NOALLOC_MAX_GROUPS;
+    // without a caller error word the kernel writes timeouts into a sink line of the array
+    // (never through a null pointer); nothing reads it
     c.d_err = d_err != nullptr ? d_err : c.d_done + pgt::kCounterStride;
     c.d_release = nullptr;
     c.d_block = nullptr;
@@ -91,7 +97,6 @@ extern "C" int pgt_gemm_noalloc(const void* A, const void* B, void* C, int64_t M
     pgt_gemm_plan_info plan;
     rc = pgt::gemm_plan(&c, &in, &d, &plan);
     if (rc) return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
     // the array keeps the previous call's contents: counters, done counter (and the error
     // word when the caller passed none) must start at zero
     const size_t clear_ints = pgt::kCounterStride * (PGT_NOALLOC_MAX_GROUPS + (d_err != nullptr ? 1 : 2));

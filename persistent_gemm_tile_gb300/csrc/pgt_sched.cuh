@@ -107,11 +107,19 @@ struct Scheduler {
     int stride;  // static: step between tile ids
     int home;    // work stealing: home group
     int cursor;  // work stealing: groups found exhausted, counted from home
+    int ahead;   // work stealing: a home-group ticket taken before the fetch that uses it
+    bool has_ahead;
+    bool stopped;  // work stealing: the home group's release flag was seen
+    static constexpr int kScan = 8;  // counters read at once by a steal scan
+    int scan[kScan];                 // work stealing: the following groups' counters, read with `ahead`
 
     __device__ __forceinline__ void init(const SchedParams& params, int worker) {
         p = params;
         home = 0;
         cursor = 0;
+        ahead = 0;
+        has_ahead = false;
+        stopped = false;
         if (p.mode == kBlocked || p.mode == kBlockedGroupedM) {
             const int B = (p.tiles + p.workers - 1) / p.workers;
             const long long s = static_cast<long long>(worker) * B;
@@ -129,36 +137,74 @@ struct Scheduler {
         }
     }
 
+    // Work stealing: the counter of the group `offset` places after home (0 past the last).
+    __device__ __forceinline__ int read_counter(int offset) const {
+        if (offset >= p.ws_groups) return 0;
+        int g = home + offset;
+        if (g >= p.ws_groups) g -= p.ws_groups;
+        return *reinterpret_cast<const volatile int*>(p.counters + g * kCounterStride);
+    }
+
+    // Work stealing: cooperative release.  A raised flag of the home group (never group 0,
+    // whose workers finish whatever is left) stops this worker before its next ticket.
+    __device__ __forceinline__ bool released() const {
+        return p.release != nullptr && home != 0 && *reinterpret_cast<const volatile int*>(p.release + home) != 0;
+    }
+
+    // Work stealing: take the home group's next ticket now, so that the atomic's round trip
+    // overlaps other work (the producer calls this a few stages before a tile's last load,
+    // and for the first tile at kernel entry); the next fetch consumes it.  The release flag
+    // is read before the ticket is taken, and a ticket taken is always used, so every tile is
+    // still handed out exactly once.  Once the home group is exhausted (stealing), tickets
+    // are taken by fetch itself.  The result register is only read by that fetch.
+    __device__ __forceinline__ void take_ahead() {
+        if (p.mode != kWorkStealing || cursor != 0 || has_ahead || stopped) return;
+        if (released()) {
+            stopped = true;
+            return;
+        }
+        ahead = atomicAdd(p.counters + home * kCounterStride, 1);
+        has_ahead = true;
+        // should the home group turn out exhausted, the steal scan starts from these reads
+        // (issued together with the atomic, so the fetch saves a round trip)
+#pragma unroll
+        for (int j = 0; j < kScan; ++j) scan[j] = read_counter(1 + j);
+    }
+
     // Next tile id, or -1 when this worker is done.
     __device__ __forceinline__ int fetch() {
         if (p.mode == kWorkStealing) {
-            // cooperative release: a raised flag of the home group (never group 0, whose
-            // workers finish whatever is left) stops this worker before its next tile
-            if (p.release != nullptr && home != 0 &&
-                *reinterpret_cast<const volatile int*>(p.release + home) != 0)
-                return -1;
             // home group first; once it is exhausted, steal from the following groups.  Counters
             // only grow during a launch, so a group whose counter already reads >= its size is
             // exhausted: the steal scan reads up to kScan counters at once (independent loads)
             // and takes an atomic ticket only where one may be left.
-            constexpr int kScan = 8;
-            while (cursor < p.ws_groups) {
+            bool pre = false;  // the first steal scan may use the counters read ahead
+            if (has_ahead) {
+                has_ahead = false;
+                if (ahead < ws_group_size(home, p.tiles, p.ws_groups, p.ws_layout))
+                    return ws_group_tile(home, ahead, p.tiles, p.ws_groups, p.ws_layout);
+                cursor = 1;
+                pre = true;
+            } else {
+                if (stopped || released()) {
+                    stopped = true;
+                    return -1;
+                }
                 if (cursor == 0) {
                     const int size = ws_group_size(home, p.tiles, p.ws_groups, p.ws_layout);
                     const int ticket = atomicAdd(p.counters + home * kCounterStride, 1);
                     if (ticket < size) return ws_group_tile(home, ticket, p.tiles, p.ws_groups, p.ws_layout);
                     cursor = 1;
-                    continue;
                 }
+            }
+            while (cursor < p.ws_groups) {
+                // Counters only grow during a launch: a value read earlier that is already at
+                // the group's size means exhausted; one below it is only a hint (the atomic
+                // decides), so reads taken ahead serve as well as fresh ones.
                 int seen[kScan];
 #pragma unroll
-                for (int j = 0; j < kScan; ++j) {
-                    int g = home + cursor + j;
-                    while (g >= p.ws_groups) g -= p.ws_groups;
-                    seen[j] = cursor + j < p.ws_groups
-                                  ? *reinterpret_cast<const volatile int*>(p.counters + g * kCounterStride)
-                                  : 0;
-                }
+                for (int j = 0; j < kScan; ++j) seen[j] = pre ? scan[j] : read_counter(cursor + j);
+                pre = false;
                 // invariant: seen[j] belongs to the group `cursor` points at in step j
 #pragma unroll
                 for (int j = 0; j < kScan; ++j) {
@@ -181,16 +227,29 @@ struct Scheduler {
         return t;
     }
 
+    // Static modes only: the next tiles of this worker's order, at most `max` of them.  They
+    // form the run first, first + step, first + 2 step, ...; returns how many (0 when done).
+    __device__ __forceinline__ int fetch_run(int max, int& first, int& step) {
+        first = next;
+        step = stride;
+        if (next >= end) return 0;
+        const int left = (end - next + stride - 1) / stride;
+        const int n = left < max ? left : max;
+        next += n * stride;
+        return n;
+    }
+
     // Work stealing: called once by every worker after its last fetch.  The last worker
     // to finish returns every counter to zero for the next launch.
+    // The done counter's add releases this worker's tickets and acquires those of the workers
+    // that finished before it, so the last one resets counters no other worker still uses;
+    // the next launch (a later kernel) sees the zeros.
     __device__ __forceinline__ void finish() {
         if (p.mode != kWorkStealing) return;
-        __threadfence();
-        const int prev = atomicAdd(p.done, 1);
+        const int prev = atom_add_acq_rel_gpu(p.done, 1);
         if (prev == p.workers - 1) {
-            for (int g = 0; g < p.ws_groups; ++g) atomicExch(p.counters + g * kCounterStride, 0);
-            atomicExch(p.done, 0);
-            __threadfence();
+            for (int g = 0; g < p.ws_groups; ++g) st_relaxed_gpu(p.counters + g * kCounterStride, 0);
+            st_relaxed_gpu(p.done, 0);
         }
     }
 };

@@ -52,6 +52,13 @@ static int cpu_checks(void) {
     d.M = 8192; d.N = 8192; d.K = 8192; d.dtype = PGT_MXFP8; d.b_layout = PGT_B_NK;
     if (pgt_gemm_workspace_bytes(&d) != 2u * 16u * 64u * 512u) { printf("FAIL mxfp8 workspace size\n"); ++failures; }
     if (strcmp(pgt_strerror(PGT_ERR_TIMEOUT), "device wait timed out") != 0) { printf("FAIL strerror\n"); ++failures; }
+    /* the flat form checks its counter-group count before anything else */
+    expect("flat ws_groups 65", pgt_gemm(NULL, NULL, NULL, NULL, NULL, NULL, 64, 64, 64, PGT_BF16, PGT_B_KN,
+                                         PGT_WORK_STEALING, 16, 65, NULL, 0, NULL), PGT_ERR_GROUPS);
+    expect("flat ws_groups -1", pgt_gemm(NULL, NULL, NULL, NULL, NULL, NULL, 64, 64, 64, PGT_BF16, PGT_B_KN,
+                                         PGT_WORK_STEALING, 16, -1, NULL, 0, NULL), PGT_ERR_GROUPS);
+    expect("flat null context", pgt_gemm(NULL, NULL, NULL, NULL, NULL, NULL, 64, 64, 64, PGT_BF16, PGT_B_KN,
+                                         PGT_WORK_STEALING, 16, 8, NULL, 0, NULL), PGT_ERR_ARG);
     return failures;
 }
 
@@ -77,8 +84,8 @@ static int gpu_checks(void) {
     cudaMemcpy(dB, hB, sizeof(uint16_t) * K * N, cudaMemcpyHostToDevice);
     for (int m = 0; m < 6; ++m) {
         cudaMemset(dC, 0xFF, sizeof(uint16_t) * M * N);
-        expect("gemm ones", pgt_gemm(ctx, dA, dB, NULL, NULL, dC, M, N, K, PGT_BF16, PGT_B_KN, modes[m], 4, NULL, 0,
-                                     NULL), PGT_OK);
+        expect("gemm ones", pgt_gemm(ctx, dA, dB, NULL, NULL, dC, M, N, K, PGT_BF16, PGT_B_KN, modes[m], 4, 0, NULL,
+                                     0, NULL), PGT_OK);
         cudaMemcpy(hC, dC, sizeof(uint16_t) * M * N, cudaMemcpyDeviceToHost);
         int bad = 0;
         for (int i = 0; i < M * N; ++i) bad += hC[i] != bf16_of((float)K);
@@ -91,8 +98,8 @@ static int gpu_checks(void) {
     cudaMemcpy(dA, hA, sizeof(uint16_t) * M * K, cudaMemcpyHostToDevice);
     cudaMemcpy(dB, hB, sizeof(uint16_t) * K * N, cudaMemcpyHostToDevice);
     for (int m = 0; m < 6; ++m) {
-        expect("gemm random", pgt_gemm(ctx, dA, dB, NULL, NULL, dC, M, N, K, PGT_BF16, PGT_B_KN, modes[m], 16, NULL,
-                                       0, NULL), PGT_OK);
+        expect("gemm random", pgt_gemm(ctx, dA, dB, NULL, NULL, dC, M, N, K, PGT_BF16, PGT_B_KN, modes[m], 16,
+                                       m == 3 ? 3 : 0, NULL, 0, NULL), PGT_OK);
         cudaMemcpy(m == 0 ? hR : hC, dC, sizeof(uint16_t) * M * N, cudaMemcpyDeviceToHost);
         if (m > 0 && memcmp(hR, hC, sizeof(uint16_t) * M * N) != 0) {
             printf("FAIL mode %d differs from blocked\n", modes[m]);
@@ -144,6 +151,8 @@ static int gpu_checks(void) {
         if (hx[i] != (float)i) { printf("FAIL add at %d\n", i); ++failures; break; }
     int32_t detail[4];
     expect("last_error", pgt_last_error(ctx, NULL, detail), PGT_OK);
+    expect("flat ws_groups above max_groups", pgt_gemm(ctx, dA, dB, NULL, NULL, dC, M, N, K, PGT_BF16, PGT_B_KN,
+                                                       PGT_WORK_STEALING, 16, 9, NULL, 0, NULL), PGT_ERR_GROUPS);
     expect("bad ws_groups", pgt_gemm_plan(ctx, &(pgt_gemm_desc){.M = 64, .N = 64, .K = 64, .group_size = 1,
                                                                    .ws_groups = 9}, &(pgt_gemm_plan_info){0}),
            PGT_ERR_GROUPS);

@@ -63,7 +63,7 @@ def test_binding_constants_match_header():
 
 def test_struct_sizes_match_c_layout():
     assert ctypes.sizeof(pgt.GemmDesc) == 6 * 8 + 10 * 4 + 8
-    assert ctypes.sizeof(pgt.PlanInfo) == 14 * 4
+    assert ctypes.sizeof(pgt.PlanInfo) == 15 * 4
     assert ctypes.sizeof(pgt.Trace) == 32
     assert ctypes.sizeof(pgt.ScaleSpace) == 2 * 8 + 4 * 8 + 8
 
@@ -84,6 +84,18 @@ def test_null_arguments_rejected_without_touching_a_gpu(lib):
     assert lib.pgt_preamble(0, 0, 0, ctypes.byref(h)) == pgt.ERR_ARG  # max_groups < 1
     assert lib.pgt_preamble(0, 65, 0, ctypes.byref(h)) == pgt.ERR_ARG
     assert lib.pgt_preamble(0, 8, 4, ctypes.byref(h)) == pgt.ERR_ARG  # unknown flag
+
+
+def test_flat_gemm_checks_counter_groups_first(lib):
+    """pgt_gemm's ws_groups must lie in [0, 64] whatever the context; a valid count with no
+    context is an argument error."""
+    def flat(ws_groups):
+        return lib.pgt_gemm(None, None, None, None, None, None, 64, 64, 64, pgt.BF16, pgt.B_KN, pgt.WORK_STEALING,
+                            16, ws_groups, None, 0, None)
+    assert flat(65) == pgt.ERR_GROUPS
+    assert flat(-1) == pgt.ERR_GROUPS
+    assert flat(0) == pgt.ERR_ARG
+    assert flat(64) == pgt.ERR_ARG
 
 
 def test_mxfp8_workspace_bytes_per_configuration(lib):

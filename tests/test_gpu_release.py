@@ -55,6 +55,7 @@ def test_gemm_release_from_start_same_bits(ctx, cfg):
     visits, _ = tb.read()
     cs = plan["cluster_size"]
     wv = [visits[w * cs] for w in range(plan["workers"])]
+    assert plan["ws_groups"] == 8
     S.check_ws_trace([[t for (t, _, _, _) in v] for v in wv], plan["tiles"], 8)
     assert all(len(v) == 0 for w, v in enumerate(wv) if w % 8 != 0)
 

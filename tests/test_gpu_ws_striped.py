@@ -79,7 +79,7 @@ def test_gemm_bit_identical_to_static_with_valid_trace(ctx, cfg, M, N, K):
         visits, _ = tb.read()
         cs = plan["cluster_size"]
         wv = [visits[w * cs] for w in range(plan["workers"])]
-        S.check_ws_trace([[t for (t, _, _, _) in v] for v in wv], plan["tiles"], G_ws, S.WS_STRIPED)
+        S.check_ws_trace([[t for (t, _, _, _) in v] for v in wv], plan["tiles"], plan["ws_groups"], S.WS_STRIPED)
         if cs == 2:  # both CTAs of a pair visit the same tiles
             assert [[t for (t, _, _, _) in visits[w * 2 + 1]] for w in range(plan["workers"])] == \
                    [[t for (t, _, _, _) in v] for v in wv]
