@@ -66,9 +66,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cfg", type=int, default=0, help="kernel configuration (PGT_CFG_*), 0 = auto")
-    ap.add_argument("--kernel", default="gemm", choices=["gemm", "add", "mxfp8"],
+    ap.add_argument("--kernel", default="gemm", choices=["gemm", "add", "mxfp8", "ragged"],
                     help="headline kernel: the bf16 GEMM (default), or the persistent add / the MXFP8 GEMM "
-                         "(for timing and profiling those kernels alone)")
+                         "(for timing and profiling those kernels alone), or one launch per scheduler and "
+                         "configuration of the ragged set (for profiling)")
     ap.add_argument("--no-extras", action="store_true", help="headline only")
     ap.add_argument("--sched", default="swizzled",
                     choices=["blocked", "interleaved", "swizzled", "work_stealing", "blocked_grouped_m",
@@ -77,6 +78,10 @@ def parse():
     ap.add_argument("--ws-groups", type=int, default=8, help="work-stealing counter groups of the bf16 headline GEMM")
     ap.add_argument("--ws-layout", default="ranges", choices=["ranges", "striped"],
                     help="work-stealing tile ownership of the bf16 headline GEMM")
+    ap.add_argument("--add-tile", default="wide", help="tile of the --kernel add headline: 'wide' (8x1024) or RxC, "
+                                                         "e.g. 32x16 (the page's tile)")
+    ap.add_argument("--add-sched", default="blocked", choices=["blocked", "interleaved"],
+                    help="scheduler of the --kernel add headline")
     ap.add_argument("--no-ragged", action="store_true",
                     help="skip the ragged-tail GEMM set (timed per scheduler, with tail idle from traces)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
@@ -97,52 +102,81 @@ def load_peaks():
 
 
 class Clocks:
-    """nvidia-smi sampling of SM clocks and throttle reasons around a timed region."""
+    """nvidia-smi sampling of SM clocks and throttle reasons.  Samples carry nvidia-smi's
+    timestamp; ``stop`` keeps only those taken between ``begin()`` and ``end()`` (host time
+    just before the first timed launch is enqueued and just after the last one has
+    finished), so the figures describe the timed launches.  A region shorter than the
+    sampling period may hold no sample: then ``samples`` is 0 and the figures are null,
+    while ``*_around`` give the samples taken around it."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, device_index: int):
+    def __init__(self, device_index: int, period_ms: int = 20):
         self.dev = device_index
+        self.period_ms = period_ms
         self.proc = None
+        self.t_begin = self.t_end = None
         self.path = os.path.join(tempfile.gettempdir(), f"pgt_clocks_{os.getpid()}.csv")
 
     def start(self):
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
             time.sleep(0.15)
         except (OSError, FileNotFoundError):
             self.proc = None
 
+    def begin(self):
+        self.t_begin = time.time()
+
+    def end(self):
+        self.t_end = time.time()
+
+    @staticmethod
+    def _parse_time(text: str):
+        import datetime
+        try:
+            return datetime.datetime.strptime(text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
     def stop(self) -> dict:
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         time.sleep(0.15)
         self.proc.terminate()
         self.proc.wait()
         self.f.close()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
+                    sm, smax = float(parts[2]), float(parts[3])
                 except ValueError:
                     continue
-                for name, val in zip(names, parts[5:9]):
-                    if val.lower().startswith("active"):
-                        reasons.add(name)
+                active = {n for n, v in zip(self.REASONS, parts[6:10]) if v.lower().startswith("active")}
+                rows.append((self._parse_time(parts[0]), sm, smax, active))
         os.unlink(self.path)
-        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        inside = [r for r in rows if r[0] is not None and self.t_begin is not None and self.t_end is not None
+                  and self.t_begin <= r[0] <= self.t_end]
+
+        def summary(rs):
+            return (float(np.median([r[1] for r in rs])) if rs else None,
+                    sorted(set().union(*[r[3] for r in rs])) if rs else [])
+        sm_in, reasons_in = summary(inside)
+        sm_all, reasons_all = summary(rows)
+        return {"sm_mhz": sm_in, "sm_max_mhz": max((r[2] for r in rows), default=None), "reasons": reasons_in,
+                "samples": len(inside), "period_ms": self.period_ms,
+                "region_s": (self.t_end - self.t_begin) if self.t_begin and self.t_end else None,
+                "sm_mhz_around": sm_all, "reasons_around": reasons_all, "samples_around": len(rows)}
 
 
 def dist_setup(args):
@@ -206,6 +240,23 @@ def time_sustained(torch, launch, seconds: float, block: int = 50) -> list:
         b.synchronize()
         out.append(a.elapsed_time(b) / block)
     return out
+
+
+def time_protocol(torch, launch, flush, warmup: int = 10, reps: int = 50) -> list:
+    """The measurement protocol of the benchmark plan: `warmup` untimed launches, then `reps`
+    launches each bracketed by its own CUDA events on the current stream, with `flush` (a
+    write larger than L2) before each one, outside the events.  Returns per-launch ms."""
+    for _ in range(warmup):
+        launch()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in evs:
+        flush()
+        a.record()
+        launch()
+        b.record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
 
 
 def tail_idle(times_ns: np.ndarray) -> float:
@@ -310,10 +361,16 @@ def run_ours(args, world, rank, local, pg):
     device = torch.device("cuda", local)
     peaks = load_peaks()
     ctx = pgt.Context(local, max_groups=16)
+    if args.kernel == "add":
+        return run_add_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peaks)
+    if args.kernel == "ragged":
+        return run_ragged_launches(args, pgt, ctx, device)
+    dC = torch.empty((M, N), dtype=torch.int16, device=device)
+    if args.kernel == "mxfp8":
+        return run_mx_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peaks, dC)
     A, B = synthetic.gemm_bf16_inputs(M, N, K, seed=2, dist="normal")
     dA = torch.from_numpy(A.view(np.int16)).to(device)
     dB = torch.from_numpy(B.view(np.int16)).to(device)
-    dC = torch.empty((M, N), dtype=torch.int16, device=device)
 
     def desc_for(mode, cfg=args.cfg):
         return pgt.make_desc(M, N, K, b_layout=pgt.B_KN, sched_mode=mode, group_size=16, ws_groups=8,
@@ -324,10 +381,6 @@ def run_ours(args, world, rank, local, pg):
         M, N, K, b_layout=pgt.B_KN, sched_mode=pgt.SCHED[args.sched], group_size=args.group,
         ws_groups=args.ws_groups, kernel_cfg=args.cfg,
         ws_layout=pgt.WS_STRIPED if args.ws_layout == "striped" else pgt.WS_RANGES)
-    if args.kernel == "add":
-        return run_add_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peaks)
-    if args.kernel == "mxfp8":
-        return run_mx_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peaks, dC)
     plan = ctx.gemm_plan(head)
     launch = lambda: ctx.gemm_ex(head, dA, dB, dC)  # noqa: E731
 
@@ -339,8 +392,10 @@ def run_ours(args, world, rank, local, pg):
     torch.cuda.synchronize()
     clocks = Clocks(local)
     clocks.start()
+    clocks.begin()
     total_ms, per = time_launches(torch, launch, args.steps, 0)
     torch.cuda.synchronize()
+    clocks.end()
     clk = clocks.stop()
     barrier(pg)
     rc, detail = ctx.last_error()
@@ -372,25 +427,31 @@ def run_ours(args, world, rank, local, pg):
     if rank != 0:
         return
     if not args.no_extras:
-        extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out)
+        extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out, head)
     print(json.dumps(out), flush=True)
     ctx.close()
 
 
 def run_add_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peaks):
-    """The persistent add (wide tile, blocked) as the timed kernel: GB/s against HBM."""
+    """The persistent add as the timed kernel (tile and order from --add-tile / --add-sched):
+    GB/s against HBM."""
     import synthetic
     x, y = synthetic.add_inputs(ADD_ROWS, ADD_COLS, seed=1)
     tx, ty = torch.from_numpy(x).to(device), torch.from_numpy(y).to(device)
     to = torch.empty_like(tx)
-    launch = lambda: ctx.add(tx, ty, to, sched_mode=pgt.BLOCKED)  # noqa: E731
+    tile = (0, 0) if args.add_tile == "wide" else tuple(int(v) for v in args.add_tile.split("x"))
+    tname = "wide 8x1024" if tile == (0, 0) else f"{tile[0]}x{tile[1]}"
+    mode = pgt.SCHED[args.add_sched]
+    launch = lambda: ctx.add(tx, ty, to, sched_mode=mode, tile_r=tile[0], tile_c=tile[1])  # noqa: E731
     for _ in range(args.warmup):
         launch()
     torch.cuda.synchronize()
     barrier(pg)
     clocks = Clocks(local)
     clocks.start()
+    clocks.begin()
     total_ms, per = time_launches(torch, launch, args.steps, 0)
+    clocks.end()
     clk = clocks.stop()
     barrier(pg)
     total_ms = max_over_ranks(pg, total_ms, device)
@@ -400,7 +461,7 @@ def run_add_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peak
            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
            "dtype": "f32", "data": "synthetic",
-           "config": {"workload": "fp32 add 8192x8192, wide 8x1024 tile, blocked", "l2": L2_NOTE},
+           "config": {"workload": f"fp32 add 8192x8192, {tname} tile, {args.add_sched}", "l2": L2_NOTE},
            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                         "frac": achieved / peaks["hbm_gbs"], "traffic": None},
            "gpu_launches": args.steps, "clocks": clk}
@@ -426,7 +487,9 @@ def run_mx_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peaks
     barrier(pg)
     clocks = Clocks(local)
     clocks.start()
+    clocks.begin()
     total_ms, per = time_launches(torch, launch, args.steps, 0)
+    clocks.end()
     clk = clocks.stop()
     barrier(pg)
     total_ms = max_over_ranks(pg, total_ms, device)
@@ -448,10 +511,34 @@ def run_mx_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peaks
     ctx.close()
 
 
-def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
+def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out, head):
     import synthetic
     A_host = dA.cpu().numpy().view(np.uint16)
     B_host = dB.cpu().numpy().view(np.uint16)
+    launch = lambda: ctx.gemm_ex(head, dA, dB, dC)  # noqa: E731
+    # the headline GEMM over a 2-second back-to-back loop, clocks sampled inside it: the
+    # power-capped steady state, against the sustained peak
+    clocks = Clocks(device.index or 0, period_ms=50)
+    clocks.start()
+    clocks.begin()
+    blocks = time_sustained(torch, launch, 2.0)
+    clocks.end()
+    clk = clocks.stop()
+    ms = float(np.median(blocks))
+    tf = FLOP / (ms * 1e-3) / 1e12
+    out["sustained"] = {"tflops": tf, "ms": ms, "seconds": 2.0, "launches": 50 * len(blocks),
+                        "peak": peaks["bf16_sustained"], "frac": tf / peaks["bf16_sustained"],
+                        "peak_kind": f"sustained bf16 ({peaks['source']})", "clocks": clk,
+                        "tflops_per_sm_ghz": tf / (clk["sm_mhz"] / 1e3) if clk.get("sm_mhz") else None}
+    # the benchmark plan's protocol: 10 warm-ups, 50 individually timed launches, L2 flushed
+    # (256 MiB written) before each; median and best
+    flush_buf = torch.empty(64 << 20, dtype=torch.float32, device=device)
+    per = time_protocol(torch, launch, lambda: flush_buf.fill_(1.0))
+    del flush_buf
+    out["protocol"] = {"warmup": 10, "reps": 50, "l2_flush": "256 MiB written before each launch, outside the events",
+                       "median_ms": float(np.median(per)), "min_ms": float(np.min(per)),
+                       "tflops_median": FLOP / (float(np.median(per)) * 1e-3) / 1e12,
+                       "tflops_best": FLOP / (float(np.min(per)) * 1e-3) / 1e12}
     # per scheduler mode: 1-second back-to-back loops, modes interleaved over 3 rounds so that
     # each sees the same mix of power and clock states (the GPU is power-capped within a
     # fraction of a second); median of the 50-launch block means
@@ -591,6 +678,28 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
                       "peak_kind": f"2 x measured bf16 burst ({peaks['source']}), nominal fp8/bf16 ratio"}
     mx["workload"] = f"MXFP8 {M}^3, E4M3 payload N(0,1), E8M0 per 1x128 K block, exps U{{-4..4}}, seed 4, " \
                      "swizzled group 16; time includes the per-call scale repack"
+    # cuBLAS MXFP8 on the same operands, rounds interleaved with this library's AUTO kernel
+    lib_launch, lib_out = cublas_mxfp8(torch, qa, sa, qb, sb, device)
+    if lib_launch is None:
+        mx["vs_cublas"] = {"unavailable": lib_out}
+    else:
+        d = pgt.make_desc(M, N, K, dtype=pgt.MXFP8, b_layout=pgt.B_NK, sched_mode=pgt.SWIZZLED, group_size=16)
+        ws = torch.empty(ctx.gemm_workspace_bytes(d), dtype=torch.uint8, device=device)
+        ours = lambda: ctx.gemm_ex(d, tqa, tqb, dC, sfa=tsa, sfb=tsb, workspace=ws)  # noqa: E731
+        ours()
+        torch.cuda.synchronize()
+        same = bool(torch.equal(dC.view(torch.bfloat16), lib_out))
+        vs = {"ours": [], "cublas": []}
+        for _ in range(6):
+            vs["ours"].extend(time_launches(torch, ours, 10, 2)[1])
+            vs["cublas"].extend(time_launches(torch, lib_launch, 10, 2)[1])
+        mx["vs_cublas"] = {k: {"tflops": FLOP / (float(np.median(v)) * 1e-3) / 1e12, "ms": float(np.median(v))}
+                           for k, v in vs.items()}
+        mx["vs_cublas"]["ratio"] = mx["vs_cublas"]["ours"]["tflops"] / mx["vs_cublas"]["cublas"]["tflops"]
+        mx["vs_cublas"]["bit_identical_outputs"] = same
+        mx["vs_cublas"]["how"] = "torch._scaled_mm, E8M0 scales repeated per 32-wide K block, bf16 out"
+        del ws
+    del lib_launch, lib_out
     out["mxfp8"] = mx
     del tqa, tsa, tqb, tsb
     if not args.no_ragged:
@@ -642,6 +751,43 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out):
     out["cpu_baseline"] = cpu_baseline(args.cpu_seconds, A_host, B_host)
 
 
+def block_scale_tiles(s: np.ndarray) -> np.ndarray:
+    """E8M0 scales (rows x blocks) in the tiled layout the library's block-scaled GEMMs read:
+    128-row x 4-block tiles of 512 bytes, tile-major over (row tile, block tile), inside a
+    tile byte (r mod 32) * 16 + ((r mod 128) div 32) * 4 + (block mod 4); padding zero."""
+    R, C = s.shape
+    Rp, Cp = -(-R // 128) * 128, -(-C // 4) * 4
+    pad = np.zeros((Rp, Cp), np.uint8)
+    pad[:R, :C] = s
+    r = np.arange(Rp)[:, None]
+    c = np.arange(Cp)[None, :]
+    off = ((r // 128) * (Cp // 4) + c // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + c % 4
+    out = np.empty(Rp * Cp, np.uint8)
+    out[off.ravel()] = pad.ravel()
+    return out
+
+
+def cublas_mxfp8(torch, qa, sa, qb, sb, device):
+    """cuBLAS's MXFP8 GEMM (torch._scaled_mm) on the same operands, as a measured point of
+    comparison (never on the path).  The library takes one E8M0 scale per 32-wide K block,
+    so each 128-wide block's scale is repeated four times: the same products exactly.
+    Returns (launch, output) or (None, reason)."""
+    try:
+        a8 = torch.from_numpy(qa).to(device).view(torch.float8_e4m3fn)
+        b8 = torch.from_numpy(qb).to(device).view(torch.float8_e4m3fn)
+        s_a = torch.from_numpy(block_scale_tiles(np.repeat(sa, 4, axis=1))).to(device).view(torch.float8_e8m0fnu)
+        s_b = torch.from_numpy(block_scale_tiles(np.repeat(sb, 4, axis=1))).to(device).view(torch.float8_e8m0fnu)
+        out = torch.empty((qa.shape[0], qb.shape[0]), dtype=torch.bfloat16, device=device)
+
+        def launch():
+            torch._scaled_mm(a8, b8.t(), s_a, s_b, out_dtype=torch.bfloat16, out=out)
+        launch()
+        torch.cuda.synchronize()
+        return launch, out
+    except Exception as e:  # an older torch or a GPU without the block-scaled path
+        return None, f"{type(e).__name__}: {str(e)[:200]}"
+
+
 def link_bandwidth(torch, h_in, d_in, h_out, d_out, streams) -> dict:
     """Host link bandwidth with pinned buffers: H2D alone, D2H alone, and both at once on two
     streams (GB/s, best of 3).  The copy engines and kernels that load or store host memory
@@ -678,9 +824,33 @@ def link_bandwidth(torch, h_in, d_in, h_out, d_out, streams) -> dict:
             "both_gbs": timed(both, n_in + n_out)}
 
 
+BF16_CFGS = ((0, "auto"), (1, "1cta_128x128"), (2, "1cta_128x256"), (3, "2cta_256x128"), (4, "2cta_256x256"))
+RAGGED = [(4864, 4096, 2048), (128, 16384, 16384), (3000, 5000, 1024)]
+
+
+def graph_us(torch, fn, reps: int = 50) -> float:
+    """Device time per call of `fn` replayed from a CUDA graph of `reps` calls (us)."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return 1e3 * e0.elapsed_time(e1) / (5 * reps)
+
+
 def small_256(torch, pgt, ctx, device):
-    """bf16 256^3 (U[-1,1], seed 0) on 128 x 128 tiles (4 tiles, 4 workers): latency per
-    scheduler in microseconds; launch-bound, so no roofline fraction is claimed."""
+    """bf16 256^3 (U[-1,1], seed 0): per scheduler on 128 x 128 tiles (4 tiles, 4 workers),
+    and per kernel configuration (swizzled, group 2) incl. AUTO; latency in microseconds,
+    eager and replayed from a CUDA graph.  Launch-bound: no roofline fraction is claimed."""
     import synthetic
     a, b = synthetic.gemm_bf16_inputs(256, 256, 256, seed=0, dist="uniform")
     ta = torch.from_numpy(a.view(np.int16)).to(device)
@@ -691,34 +861,26 @@ def small_256(torch, pgt, ctx, device):
                        (pgt.WORK_STEALING, "work_stealing"), (pgt.LAUNCH_CONTROL, "launch_control")):
         d = pgt.make_desc(256, 256, 256, sched_mode=mode, group_size=2, kernel_cfg=pgt.CFG_1CTA_128x128)
         _, per = time_launches(torch, lambda: ctx.gemm_ex(d, ta, tb_, tc), 50, 5)
-        # the same launches captured in a CUDA graph and replayed: device time per GEMM
-        reps = 50
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for _ in range(reps):
-                ctx.gemm_ex(d, ta, tb_, tc)
-        g.replay()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(5):
-            g.replay()
-        e1.record()
-        torch.cuda.synchronize()
-        res[name] = {"us_eager": 1e3 * float(np.median(per)), "us_graph": 1e3 * e0.elapsed_time(e1) / (5 * reps)}
+        res[name] = {"us_eager": 1e3 * float(np.median(per)), "us_graph": graph_us(torch, lambda: ctx.gemm_ex(d, ta, tb_, tc))}
+    per_cfg = {}
+    for cfg, cname in BF16_CFGS:
+        d = pgt.make_desc(256, 256, 256, sched_mode=pgt.SWIZZLED, group_size=2, kernel_cfg=cfg)
+        per_cfg[cname] = {"us_graph": graph_us(torch, lambda: ctx.gemm_ex(d, ta, tb_, tc)),
+                          "kernel_cfg": ctx.gemm_plan(d)["kernel_cfg"]}
+    res["per_cfg"] = per_cfg
     return res
 
 
 def ragged_set(torch, pgt, ctx, device):
-    """The ragged-tail set (tile counts not a multiple of the SM count), every scheduler:
-    TFLOP/s and tail idle (1 - busy / (workers * span)) from a traced launch."""
+    """The ragged-tail set (tile counts not a multiple of the SM count), every kernel
+    configuration (AUTO included) and every scheduler: TFLOP/s and tail idle
+    (1 - busy / (workers * span)) from a traced launch."""
     import synthetic
-    shapes = [(4864, 4096, 2048), (128, 16384, 16384), (3000, 5000, 1024)]
     res = {}
     names = {pgt.BLOCKED: "blocked", pgt.INTERLEAVED: "interleaved", pgt.SWIZZLED: "swizzled",
              pgt.WORK_STEALING: "work_stealing", pgt.BLOCKED_GROUPED_M: "blocked_grouped_m",
              pgt.LAUNCH_CONTROL: "launch_control"}
-    for (m, n, k), (a, b) in zip(shapes, synthetic.gemm_bf16_sequence(shapes, seed=3, dist="uniform")):
+    for (m, n, k), (a, b) in zip(RAGGED, synthetic.gemm_bf16_sequence(RAGGED, seed=3, dist="uniform")):
         ta = torch.from_numpy(a.view(np.int16)).to(device)
         tb_ = torch.from_numpy(b.view(np.int16)).to(device)
         tc = torch.empty((m, n), dtype=torch.int16, device=device)
@@ -726,7 +888,7 @@ def ragged_set(torch, pgt, ctx, device):
         res[key] = {}
         variants = [(mode, name, pgt.WS_RANGES) for mode, name in names.items()]
         variants.append((pgt.WORK_STEALING, "work_stealing_striped", pgt.WS_STRIPED))
-        for cfg, cname in ((pgt.CFG_1CTA_128x256, "1cta_128x256"), (pgt.CFG_2CTA_256x128, "2cta_256x128")):
+        for cfg, cname in BF16_CFGS:
             for mode, name, layout in variants:
                 d = pgt.make_desc(m, n, k, b_layout=pgt.B_KN, sched_mode=mode, group_size=16, ws_groups=8,
                                   kernel_cfg=cfg, ws_layout=layout)
@@ -738,9 +900,49 @@ def ragged_set(torch, pgt, ctx, device):
                 torch.cuda.synchronize()
                 res[key][f"{cname}_{name}"] = {"tflops": 2.0 * m * n * k / (ms * 1e-3) / 1e12, "ms": ms,
                                                "tail_idle": tail_idle(tr.times.cpu().numpy()),
-                                               "tiles": plan["tiles"], "workers": plan["workers"]}
+                                               "tiles": plan["tiles"], "workers": plan["workers"],
+                                               "kernel_cfg": plan["kernel_cfg"]}
+        # AUTO against the fastest configuration under the swizzled order
+        sw = {c: res[key][f"{c}_swizzled"]["tflops"] for _, c in BF16_CFGS if c != "auto"}
+        best = max(sw, key=sw.get)
+        res[key]["auto_vs_best"] = {"best": best, "auto_frac_of_best": res[key]["auto_swizzled"]["tflops"] / sw[best]}
         del ta, tb_, tc
     return res
+
+
+def run_ragged_launches(args, pgt, ctx, device):
+    """--kernel ragged: one untraced launch per (shape, configuration, scheduler) of the
+    ragged set, in a fixed order, for a profiler to capture (e.g. SM-active against elapsed
+    cycles per launch); prints the launch order as one JSON line."""
+    import torch
+
+    import synthetic
+    order = []
+    modes = ((pgt.BLOCKED, "blocked", pgt.WS_RANGES), (pgt.INTERLEAVED, "interleaved", pgt.WS_RANGES),
+             (pgt.SWIZZLED, "swizzled", pgt.WS_RANGES), (pgt.WORK_STEALING, "work_stealing", pgt.WS_RANGES),
+             (pgt.WORK_STEALING, "work_stealing_striped", pgt.WS_STRIPED),
+             (pgt.BLOCKED_GROUPED_M, "blocked_grouped_m", pgt.WS_RANGES),
+             (pgt.LAUNCH_CONTROL, "launch_control", pgt.WS_RANGES))
+    for (m, n, k), (a, b) in zip(RAGGED, synthetic.gemm_bf16_sequence(RAGGED, seed=3, dist="uniform")):
+        ta = torch.from_numpy(a.view(np.int16)).to(device)
+        tb_ = torch.from_numpy(b.view(np.int16)).to(device)
+        tc = torch.empty((m, n), dtype=torch.int16, device=device)
+        for cfg, cname in ((0, "auto"), (2, "1cta_128x256"), (3, "2cta_256x128")):
+            for mode, name, layout in modes:
+                d = pgt.make_desc(m, n, k, sched_mode=mode, group_size=16, ws_groups=8, kernel_cfg=cfg,
+                                  ws_layout=layout)
+                ctx.gemm_ex(d, ta, tb_, tc)
+                plan = ctx.gemm_plan(d)
+                order.append({"shape": f"{m}x{n}x{k}", "cfg": cname, "kernel_cfg": plan["kernel_cfg"],
+                              "sched": name, "tiles": plan["tiles"], "workers": plan["workers"],
+                              "ctas": plan["ctas"]})
+        torch.cuda.synchronize()
+        del ta, tb_, tc
+    rc, detail = ctx.last_error()
+    if rc != 0:
+        raise RuntimeError(f"device-side timeout: {detail}")
+    print(json.dumps({"metric": "ragged-set launches (profiling)", "launches": order}), flush=True)
+    ctx.close()
 
 
 def main():

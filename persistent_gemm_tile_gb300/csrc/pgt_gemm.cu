@@ -178,10 +178,77 @@ SfGeometry sf_geometry(int64_t M, int64_t N, int64_t K, int bn) {
     return g;
 }
 
-// The configuration PGT_CFG_AUTO stands for, per dtype.
-int resolve_cfg(int cfg, int dtype) {
-    (void)dtype;
-    return cfg == PGT_CFG_AUTO ? PGT_CFG_2CTA_256x256 : cfg;  // fastest measured for bf16 and MXFP8 alike
+// ------------------------------------------------------------- automatic configuration
+// PGT_CFG_AUTO picks, per problem, the configuration with the least predicted launch time
+//     t = a + W * (b + r * K + s * MB)  (microseconds)
+// where W = ceil(T / P) is the number of waves of tiles (T tiles on P resident workers), K
+// the reduction length, and MB the operand bytes one CTA loads per tile (its 128 rows of A
+// and its rows or columns of B over K, in millions), counted twice for an operand whose row
+// pitch is not a multiple of 128 bytes (every TMA box row then straddles two L2 lines).
+// a is the launch and pipeline fill/drain cost, b the per-tile switch, r and s the
+// mainloop.  The coefficients are fitted to launches of each configuration timed on a GB300
+// (bf16: 18 shapes, square 256 .. 8192, the ragged set, skinny M or N, short and long K; the
+// fit then picked the fastest configuration on 27 further shapes; MXFP8: 18 shapes),
+// weighting relative error.  Candidates: bf16 1-CTA 128x128, 1-CTA 128x256 and pair
+// 256x256 (the pair 256x128 is never more than a percent faster than 1-CTA 128x128, and
+// usually slower); MXFP8 the same three (the 256x224 tile repacks B's scales per tile, so it
+// would change the workspace size, and it is slower wherever measured).
+struct CostModel {
+    int cfg;
+    double a, b, r, s;
+};
+constexpr CostModel kBf16Cost[] = {
+    {PGT_CFG_1CTA_128x128, 4.4861, 0.204532, 0.00281482, 3.14444},
+    {PGT_CFG_1CTA_128x256, 4.96696, 0.562448, 0.00141099, 5.56054},
+    {PGT_CFG_2CTA_256x256, 6.78523, 1.13483, 0.00126101, 7.12013},
+};
+// MXFP8 rows are K bytes with K a multiple of 128, so the operand bytes are proportional to
+// K and fold into r (s = 0); times include the per-call scale repack.
+constexpr CostModel kMxCost[] = {
+    {PGT_CFG_1CTA_128x128, 5.98816, 0.328656, 0.00265461, 0.0},
+    {PGT_CFG_1CTA_128x256, 5.88766, 0.390631, 0.00332382, 0.0},
+    {PGT_CFG_2CTA_256x256, 6.66304, 1.33953, 0.00307062, 0.0},
+};
+
+// The configuration a workspace is sized for: AUTO only ever picks tiles whose widths are
+// multiples of 128, and those share one packed-scale layout.
+int workspace_cfg(int cfg) { return cfg == PGT_CFG_AUTO ? PGT_CFG_2CTA_256x256 : cfg; }
+
+// Resolve PGT_CFG_AUTO for `d` (leading dimensions already defaulted) on the context's device.
+int resolve_cfg(const pgt_ctx* ctx, const pgt_gemm_desc& d, int* out) {
+    if (d.kernel_cfg != PGT_CFG_AUTO) {
+        *out = d.kernel_cfg;
+        return PGT_OK;
+    }
+    const bool mx = d.dtype == PGT_MXFP8;
+    const int64_t es = mx ? 1 : 2;
+    const bool mis_a = (d.lda * es) % 128 != 0;
+    const bool mis_b = (d.ldb * es) % 128 != 0;
+    const CostModel* table = mx ? kMxCost : kBf16Cost;
+    const int n_cand = mx ? (int)(sizeof(kMxCost) / sizeof(kMxCost[0])) : (int)(sizeof(kBf16Cost) / sizeof(kBf16Cost[0]));
+    double best_t = 0.0;
+    int best = -1;
+    for (int i = 0; i < n_cand; ++i) {
+        const CostModel& cm = table[i];
+        CfgShape s;
+        if (!cfg_shape(cm.cfg, d.dtype, &s)) continue;
+        KernelInfo ki;
+        const int rc = kernel_info(ctx->device, cm.cfg, mx, d.b_layout == PGT_B_KN, false, s, &ki);
+        if (rc) return rc;
+        const int64_t tiles = cdiv64(cdiv64(d.M, 128), s.cs) * cdiv64(d.N, s.bn);
+        const int64_t workers = ki.max_workers < tiles ? ki.max_workers : tiles;
+        const double waves = (double)cdiv64(tiles, workers > 0 ? workers : 1);
+        const double mb = ((double)128 * d.K * es * (mis_a ? 2 : 1) + (double)(s.bn / s.cs) * d.K * es * (mis_b ? 2 : 1)) *
+                          1e-6;
+        const double t = cm.a + waves * (cm.b + cm.r * (double)d.K + cm.s * mb);
+        if (best < 0 || t < best_t) {
+            best_t = t;
+            best = cm.cfg;
+        }
+    }
+    if (best < 0) return PGT_ERR_UNSUPPORTED;
+    *out = best;
+    return PGT_OK;
 }
 
 }  // namespace
@@ -202,7 +269,7 @@ int encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, u
 size_t gemm_workspace_bytes(const pgt_gemm_desc& d) {
     if (d.dtype != PGT_MXFP8 || d.M < 1 || d.N < 1 || d.K < 128 || d.K % 128) return 0;
     CfgShape s;
-    if (!cfg_shape(resolve_cfg(d.kernel_cfg, d.dtype), d.dtype, &s)) return 0;
+    if (!cfg_shape(workspace_cfg(d.kernel_cfg), d.dtype, &s)) return 0;
     const SfGeometry g = sf_geometry(d.M, d.N, d.K, s.bn);
     return g.bytes_a + g.bytes_b;
 }
@@ -231,7 +298,10 @@ int gemm_plan(const pgt_ctx* ctx, const pgt_gemm_desc* in, pgt_gemm_desc* d, pgt
     if (d->dtype == PGT_MXFP8) {
         if (d->K % 128 != 0 || d->b_layout != PGT_B_NK) return PGT_ERR_ARG;
     }
-    d->kernel_cfg = resolve_cfg(d->kernel_cfg, d->dtype);
+    int cfg = 0;
+    int rc0 = resolve_cfg(ctx, *d, &cfg);
+    if (rc0) return rc0;
+    d->kernel_cfg = cfg;
     CfgShape s;
     if (!cfg_shape(d->kernel_cfg, d->dtype, &s)) return PGT_ERR_UNSUPPORTED;
     const int64_t m_blocks = cdiv64(d->M, 128);
@@ -254,6 +324,8 @@ int gemm_plan(const pgt_ctx* ctx, const pgt_gemm_desc* in, pgt_gemm_desc* d, pgt
         if (workers < 1) workers = 1;
     }
     if (workers * s.cs >= lim) return PGT_ERR_ARG;
+    // every counter group gets a home worker (a group without one would only be stolen from)
+    if (d->ws_groups > workers) d->ws_groups = (int32_t)workers;
     p->kernel_cfg = d->kernel_cfg;
     p->bm = 128;
     p->bn = s.bn;
@@ -268,6 +340,7 @@ int gemm_plan(const pgt_ctx* ctx, const pgt_gemm_desc* in, pgt_gemm_desc* d, pgt
     p->ctas = (int32_t)(workers * s.cs);
     p->k_iters = (int32_t)cdiv64(d->K, s.bk);
     p->smem_bytes = s.smem;
+    p->ws_groups = d->ws_groups;
     return PGT_OK;
 }
 
