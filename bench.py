@@ -259,15 +259,18 @@ def time_protocol(torch, launch, flush, warmup: int = 10, reps: int = 50) -> lis
     return [a.elapsed_time(b) for a, b in evs]
 
 
-def tail_idle(times_ns: np.ndarray) -> float:
+def tail_idle(times_ns: np.ndarray, slots: int | None = None) -> float:
     """1 - sum(busy) / (P * span): the share of worker time spent idle in the launch, over
     the workers that ran (under launch control most launched workers are cancelled before
-    they start and record no times)."""
+    they start and record no times).  With `slots` (e.g. the SM count, one CTA per SM), the
+    idle share of that many slots instead: the quantity ncu's 1 - sm__cycles_active.avg /
+    sm__cycles_elapsed.max measures, SMs that ran no CTA counting as idle."""
     t = times_ns[(times_ns[:, 0] > 0) & (times_ns[:, 1] > 0)]
     if len(t) == 0:
         return float("nan")
     span = float(t[:, 1].max() - t[:, 0].min())
-    return 1.0 - float((t[:, 1] - t[:, 0]).sum()) / (len(t) * span) if span > 0 else 0.0
+    n = len(t) if slots is None else slots
+    return 1.0 - float((t[:, 1] - t[:, 0]).sum()) / (n * span) if span > 0 else 0.0
 
 
 def cpu_baseline(budget_s: float, A_bits, B_bits, rows_hint: int | None = None) -> dict:
@@ -636,6 +639,16 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out, head
             add[f"{tname}_{mname}"] = {"gbs": gbs, "ms": ms}
             if best is None or gbs > best[1]:
                 best = (f"{tname}_{mname}", gbs, ms)
+    # the page's 32 x 16 tile against the worker count (0 = the library's default); the SM
+    # count is the pages' own choice
+    sweep = {}
+    for mode, mname in ((pgt.BLOCKED, "blocked"), (pgt.INTERLEAVED, "interleaved")):
+        for P in (0, ctx.num_sms, 512, 1024, 2048, 4096):
+            fn = lambda: ctx.add(tx, ty, to, sched_mode=mode, tile_r=32, tile_c=16, num_workers=P)  # noqa: E731
+            _, per = time_launches(torch, fn, 20, 3)
+            sweep[f"{mname}_{P or 'default'}"] = ADD_BYTES / (float(np.median(per)) * 1e-3) / 1e9
+        sweep[f"{mname}_default_workers"] = ctx.add_workers(ADD_ROWS, ADD_COLS, 32, 16, sched_mode=mode)
+    add["page_32x16_workers_gbs"] = sweep
     add["roofline"] = {"bound": "hbm", "achieved": best[1], "peak": peaks["hbm_gbs"], "unit": "GB/s",
                        "frac": best[1] / peaks["hbm_gbs"],
                        "traffic": profiled_traffic("add_wide_8x1024") if best[0].startswith("wide") else None,
@@ -898,8 +911,10 @@ def ragged_set(torch, pgt, ctx, device):
                 tr = pgt.TraceBuffers(plan["ctas"], plan["tiles"], device=device)
                 ctx.gemm_ex(d, ta, tb_, tc, trace=tr.struct)
                 torch.cuda.synchronize()
+                times = tr.times.cpu().numpy()
                 res[key][f"{cname}_{name}"] = {"tflops": 2.0 * m * n * k / (ms * 1e-3) / 1e12, "ms": ms,
-                                               "tail_idle": tail_idle(tr.times.cpu().numpy()),
+                                               "tail_idle": tail_idle(times),
+                                               "tail_idle_all_sms": tail_idle(times, ctx.num_sms),
                                                "tiles": plan["tiles"], "workers": plan["workers"],
                                                "kernel_cfg": plan["kernel_cfg"]}
         # AUTO against the fastest configuration under the swizzled order

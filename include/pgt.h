@@ -290,16 +290,26 @@ int pgt_gemm_host(pgt_ctx* ctx, const pgt_gemm_desc* desc, const void* h_A, cons
  * sched_mode PGT_BLOCKED or PGT_INTERLEAVED with the linear decode (tile rows fastest).
  * tile_r in [1, 1024], tile_c in [1, 4096], tile_r * tile_c <= 65536; tile_r = tile_c = 0
  * selects the wide vectorised tile.  num_workers 0 = every CTA that fits on the GPU at
- * once.  out may alias x or y exactly; other overlaps are undefined.  The result does not
+ * once, or, for tiles narrower than a 128-byte line, the largest count that fits and keeps
+ * the tile columns sharing a line in flight together (see pgt_add_workers).  Each worker
+ * streams several of its tiles at once.  out may alias x or y exactly; other overlaps are
+ * undefined.  The result does not
  * depend on the tile, the order or the worker count.  trace as in pgt_gemm_ex (m_idx /
  * n_idx are tile row / column). */
 int pgt_add(pgt_ctx* ctx, const float* x, const float* y, float* out, int64_t rows,
             int64_t cols, int64_t ldx, int64_t ldy, int64_t ldo, int sched_mode, int tile_r,
             int tile_c, int num_workers, const pgt_trace* trace, void* stream);
 
-/* Workers pgt_add will launch for these arguments (after defaults), or a negative status. */
+/* Workers pgt_add will launch for these arguments (after defaults), or a negative status.
+ * The default for tiles narrower than 128 bytes: with tile rows fastest a worker walks down
+ * a column of tiles, and the rest of each line belongs to the neighbouring tile columns, so
+ * the count is chosen to have those read at the same time (blocked: n_tiles * j workers, j
+ * dividing the tile rows, each covering an equal part of one column, as many as fit at once;
+ * interleaved: a multiple of tile rows * tile columns per line, up to twice what fits);
+ * otherwise every CTA that fits.  Workers beyond the CTAs that fit at once run in turn on
+ * the resident CTAs (CTA b runs workers b, b + grid, ...). */
 int pgt_add_workers(const pgt_ctx* ctx, int64_t rows, int64_t cols, int tile_r, int tile_c,
-                    int num_workers);
+                    int sched_mode, int num_workers);
 
 /* ----------------------------------------------------- fused multi-space loop */
 /* One elementwise tile space: out = scale * x over a rows x cols fp32 matrix (row strides

@@ -102,7 +102,7 @@ def lib() -> ctypes.CDLL:
         L.pgt_gemm.argtypes = [P, P, P, P, P, P, I64, I64, I64, I, I, I, I, I, P, SZ, P]
         L.pgt_gemm_host.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
         L.pgt_add.argtypes = [P, P, P, P, I64, I64, I64, I64, I64, I, I, I, I, P, P]
-        L.pgt_add_workers.argtypes = [P, I64, I64, I, I, I]
+        L.pgt_add_workers.argtypes = [P, I64, I64, I, I, I, I]
         L.pgt_schedule_log.argtypes = [P, I64, I64, I, I, I, I, I, I, P, P]
         L.pgt_gemm_noalloc.argtypes = [P, P, P, I64, I64, I64, I, I, I, P, P]
         L.pgt_multi_loop.argtypes = [P, P, I, I, I, I, I, P, P]
@@ -267,8 +267,10 @@ class Context:
                                     tile_c, num_workers, ctypes.byref(trace) if trace else None, _stream(stream)),
                "pgt_multi_loop")
 
-    def add_workers(self, rows, cols, tile_r=0, tile_c=0, num_workers=0) -> int:
-        return _check(lib().pgt_add_workers(self.handle, rows, cols, tile_r, tile_c, num_workers),
+    def add_workers(self, rows, cols, tile_r=0, tile_c=0, num_workers=0, sched_mode=BLOCKED) -> int:
+        if isinstance(sched_mode, str):
+            sched_mode = SCHED[sched_mode]
+        return _check(lib().pgt_add_workers(self.handle, rows, cols, tile_r, tile_c, sched_mode, num_workers),
                       "pgt_add_workers")
 
     def schedule_log(self, m_blocks, n_blocks, cluster_size, sched_mode, group_size, ws_groups, num_workers,

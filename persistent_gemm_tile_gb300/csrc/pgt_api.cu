@@ -316,8 +316,9 @@ int pgt_add(pgt_ctx* ctx, const float* x, const float* y, float* out, int64_t ro
                       static_cast<cudaStream_t>(stream));
 }
 
-int pgt_add_workers(const pgt_ctx* ctx, int64_t rows, int64_t cols, int tile_r, int tile_c, int num_workers) {
-    return add_workers(ctx, rows, cols, tile_r, tile_c, num_workers);
+int pgt_add_workers(const pgt_ctx* ctx, int64_t rows, int64_t cols, int tile_r, int tile_c, int sched_mode,
+                    int num_workers) {
+    return add_workers(ctx, rows, cols, tile_r, tile_c, sched_mode, num_workers);
 }
 
 int pgt_schedule_log(pgt_ctx* ctx, int64_t m_blocks, int64_t n_blocks, int cluster_size, int sched_mode,

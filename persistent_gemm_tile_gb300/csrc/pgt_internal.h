@@ -46,7 +46,8 @@ int add_launch(pgt_ctx* ctx, const float* x, const float* y, float* out, int64_t
                int64_t ldx, int64_t ldy, int64_t ldo, int sched_mode, int tile_r, int tile_c,
                int num_workers, const pgt_trace* trace, cudaStream_t stream);
 
-int add_workers(const pgt_ctx* ctx, int64_t rows, int64_t cols, int tile_r, int tile_c, int num_workers);
+int add_workers(const pgt_ctx* ctx, int64_t rows, int64_t cols, int tile_r, int tile_c, int sched_mode,
+                int num_workers);
 
 int schedule_log_launch(pgt_ctx* ctx, int64_t m_blocks, int64_t n_blocks, int cluster_size,
                         int sched_mode, int group_size, int ws_groups, int ws_layout, int num_workers,

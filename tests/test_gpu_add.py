@@ -93,9 +93,12 @@ def test_add_special_values_no_flush(ctx):
 
 
 @pytest.mark.parametrize("mode", [pgt.BLOCKED, pgt.INTERLEAVED])
-@pytest.mark.parametrize("P", [1, 5, 152])
-def test_add_trace_matches_oracle_schedule(ctx, mode, P):
-    rows, cols, tr, tc = 200, 300, 32, 16
+@pytest.mark.parametrize("P,rows,cols", [(1, 200, 300), (5, 200, 300), (152, 200, 300), (3000, 200, 300),
+                                         (2500, 2048, 2048)])
+def test_add_trace_matches_oracle_schedule(ctx, mode, P, rows, cols):
+    """Per-worker visit lists equal the oracle's.  With more workers than CTAs fit on the
+    GPU (2500, 3000), each CTA runs several workers in turn."""
+    tr, tc = 32, 16
     x, y = synthetic.add_inputs(rows, cols, seed=8)
     tx, ty = torch.from_numpy(x).cuda(), torch.from_numpy(y).cuda()
     out = torch.empty_like(tx)
@@ -107,6 +110,22 @@ def test_add_trace_matches_oracle_schedule(ctx, mode, P):
     want = S.static_schedule(mode, grid, P, 1)
     assert [[(t, m, n) for (t, m, n, _) in v] for v in visits] == [[(t, m, n) for (_, t, m, n) in v] for v in want]
     assert np.array_equal(bits(out.cpu().numpy()), bits(OA.add_f32(x, y)))
+
+
+def test_default_workers_keep_line_partners_together(ctx):
+    """32 x 16 tiles are half a 128-byte line wide: the default worker count makes workers on
+    neighbouring tile columns read the same rows together (blocked: whole columns split
+    evenly, interleaved: waves of whole column pairs, two workers per resident CTA); the wide
+    tile takes every CTA that fits, whatever the order."""
+    m_tiles, n_tiles = 8192 // 32, 8192 // 16
+    P = ctx.add_workers(8192, 8192, 32, 16, sched_mode=pgt.BLOCKED)
+    assert P % n_tiles == 0 and m_tiles % (P // n_tiles) == 0, P
+    P = ctx.add_workers(8192, 8192, 32, 16, sched_mode=pgt.INTERLEAVED)
+    assert P % (2 * m_tiles) == 0 and P > n_tiles, P  # about two workers per resident CTA
+    wide = ctx.add_workers(8192, 8192, 0, 0, sched_mode=pgt.BLOCKED)
+    assert wide == ctx.add_workers(8192, 8192, 0, 0, sched_mode=pgt.INTERLEAVED)
+    assert wide % ctx.num_sms == 0
+    assert ctx.add_workers(100, 100, 32, 16, num_workers=7) == 7
 
 
 def test_add_rejects_bad_arguments(ctx):
