@@ -41,9 +41,9 @@ L2_NOTE = "inputs larger than L2: A+B+C = 384 MiB per GEMM > 129 MB L2; add x+y+
 GEMM_SOURCES = ["csrc/pgt_gemm_kernel.cuh", "csrc/pgt_device.cuh", "csrc/pgt_sched.cuh"]
 ADD_SOURCES = ["csrc/pgt_add.cu", "csrc/pgt_device.cuh", "csrc/pgt_sched.cuh"]
 PROFILED_TRAFFIC = {
-    "gemm_bf16_2cta_256x256": (9.161178e+08 + 1.285768e+08, GEMM_SOURCES, "95e9e8c757920309"),
-    "gemm_mxfp8_2cta_256x256": (2.483269e+08 + 1.173100e+08, GEMM_SOURCES, "95e9e8c757920309"),
-    "add_wide_8x1024": (5.369303e+08 + 2.296192e+08, ADD_SOURCES, "ba6a4f5c86e81ce0"),
+    "gemm_bf16_2cta_256x256": (8.73577472e+08 + 1.27464704e+08, GEMM_SOURCES, "230ce9d380f60ad1"),
+    "add_page_32x16_blocked": (5.3693696e+08 + 2.32903936e+08, ADD_SOURCES, "71df49dcd8988376"),
+    "add_page_32x16_interleaved": (5.6740352e+08 + 2.38276352e+08, ADD_SOURCES, "71df49dcd8988376"),
 }
 
 
@@ -444,6 +444,7 @@ def run_add_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peak
     to = torch.empty_like(tx)
     tile = (0, 0) if args.add_tile == "wide" else tuple(int(v) for v in args.add_tile.split("x"))
     tname = "wide 8x1024" if tile == (0, 0) else f"{tile[0]}x{tile[1]}"
+    traffic_key = f"add_page_32x16_{args.add_sched}" if tile == (32, 16) else f"add_wide_8x1024_{args.add_sched}"
     mode = pgt.SCHED[args.add_sched]
     launch = lambda: ctx.add(tx, ty, to, sched_mode=mode, tile_r=tile[0], tile_c=tile[1])  # noqa: E731
     for _ in range(args.warmup):
@@ -466,7 +467,7 @@ def run_add_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peak
            "dtype": "f32", "data": "synthetic",
            "config": {"workload": f"fp32 add 8192x8192, {tname} tile, {args.add_sched}", "l2": L2_NOTE},
            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": achieved / peaks["hbm_gbs"], "traffic": None},
+                        "frac": achieved / peaks["hbm_gbs"], "traffic": profiled_traffic(traffic_key)},
            "gpu_launches": args.steps, "clocks": clk}
     if rank == 0:
         print(json.dumps(out), flush=True)
@@ -651,7 +652,7 @@ def extras(args, torch, pgt, ctx, device, dA, dB, dC, desc_for, peaks, out, head
     add["page_32x16_workers_gbs"] = sweep
     add["roofline"] = {"bound": "hbm", "achieved": best[1], "peak": peaks["hbm_gbs"], "unit": "GB/s",
                        "frac": best[1] / peaks["hbm_gbs"],
-                       "traffic": profiled_traffic("add_wide_8x1024") if best[0].startswith("wide") else None,
+                       "traffic": profiled_traffic("add_" + best[0]),
                        "kernel": best[0],
                        "algorithmic_bytes": ADD_BYTES}
     add["workload"] = "fp32 8192x8192 x,y ~ N(0,1) seed 1, out = x + y"

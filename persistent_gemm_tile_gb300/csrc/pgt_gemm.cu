@@ -401,7 +401,8 @@ int gemm_launch(pgt_ctx* ctx, const pgt_gemm_desc& d, const pgt_gemm_plan_info& 
     gp.ldc = d.ldc;
     // K-direction period: the workers this configuration keeps resident at once (capped at
     // T), whatever the scheduler or the requested worker count, so every scheduler gives a
-    // tile the same K order.  bf16 only (MXFP8 scales are loaded in forward K groups).
+    // tile the same K order.  bf16 only: MXFP8 loads its scales in forward groups of four K
+    // blocks, and walking K backwards measured 4-8% slower for it.
     gp.kdir_period = 0;
     if (!mx) {
         KernelInfo k0;
