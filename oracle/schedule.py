@@ -43,6 +43,15 @@ counters, each over its own contiguous range, so each XCD's L2 sees one region).
 tiles ``t`` with ``t mod G_ws == g``, ticket ``j`` being tile ``j*G_ws + g``, so the
 groups advance together along the decode order.  Counters, homes, stealing, release and
 reset are unchanged.
+
+First tickets assigned at launch (``implied_first``): the page's loop takes every ticket
+from a counter; the GB300 build assigns worker ``c``'s first ticket without an atomic:
+ticket ``c div G_ws`` of its home group, which is exactly the ticket it would draw if every
+worker fetched once before any fetched twice.  The counter of group ``g`` then stands for
+tickets from ``n_g`` on, ``n_g`` being the number of workers homed on ``g``, and still
+starts at zero.  A worker released before launch keeps its assigned tile (release gates
+only the tickets drawn from counters).  The invariants of :func:`check_ws_trace` hold
+unchanged.
 """
 from __future__ import annotations
 
@@ -162,14 +171,19 @@ def ws_group_tiles(T: int, groups: int, layout: int = WS_RANGES) -> list[list[in
 
 
 class WsState:
-    """Counters plus each worker's cursor: the sequential model of the ticket protocol."""
+    """Counters plus each worker's cursor: the sequential model of the ticket protocol.
+    With ``implied_first`` each worker's first ticket is assigned at launch (module notes)."""
 
-    def __init__(self, T: int, P: int, groups: int, layout: int = WS_RANGES):
+    def __init__(self, T: int, P: int, groups: int, layout: int = WS_RANGES, implied_first: bool = False):
         self.T, self.P, self.groups = T, P, groups
         self.tiles = ws_group_tiles(T, groups, layout)
         self.counter = [0] * groups
         self.cursor = [0] * P  # groups already found exhausted, counted from home
         self.done = [False] * P
+        self.implied_first = implied_first
+        self.started = [False] * P
+        # tickets assigned at launch per group: one per worker homed there
+        self.offset = [sum(1 for c in range(P) if c % groups == g) if implied_first else 0 for g in range(groups)]
 
     def fetch(self, c: int, released=frozenset()) -> int:
         """One fetch by worker c; returns a tile id or -1 once every group is exhausted.
@@ -180,12 +194,18 @@ class WsState:
         in ``released``, stops taking tiles; group 0 is never released, so its workers
         always finish the remaining tiles by stealing."""
         home = c % self.groups
+        if self.implied_first and not self.started[c]:
+            self.started[c] = True
+            j = c // self.groups  # the ticket assigned at launch
+            if j < len(self.tiles[home]):
+                return self.tiles[home][j]
+            self.cursor[c] = 1  # home holds no ticket for this worker: all of them are assigned
         if home != 0 and home in released:
             self.done[c] = True
             return -1
         while self.cursor[c] < self.groups:
             g = (home + self.cursor[c]) % self.groups
-            ticket = self.counter[g]
+            ticket = self.counter[g] + self.offset[g]
             self.counter[g] += 1  # the atomic add
             if ticket < len(self.tiles[g]):
                 return self.tiles[g][ticket]
@@ -194,10 +214,11 @@ class WsState:
         return -1
 
 
-def ws_simulate(T: int, P: int, groups: int, pick, release_at=None, layout: int = WS_RANGES) -> list[list[int]]:
+def ws_simulate(T: int, P: int, groups: int, pick, release_at=None, layout: int = WS_RANGES,
+                implied_first: bool = False) -> list[list[int]]:
     """Run the protocol with workers fetching in the order chosen by ``pick(live) -> c``.
     ``release_at(step) -> set of released groups`` models flags raised while it runs."""
-    st = WsState(T, P, groups, layout)
+    st = WsState(T, P, groups, layout, implied_first)
     visits: list[list[int]] = [[] for _ in range(P)]
     live = list(range(P))
     step = 0

@@ -217,6 +217,94 @@ def test_ws_striped_checker_rejects_planted_mistakes(plant):
         S.check_ws_trace(visits, 60, 3, S.WS_STRIPED)
 
 
+# --------------------------------------------- first tickets assigned at launch (reading 22)
+@pytest.mark.parametrize("layout", [S.WS_RANGES, S.WS_STRIPED])
+@pytest.mark.parametrize("seed", range(6))
+def test_ws_implied_first_equals_one_round_in_worker_order(layout, seed):
+    """Assigning worker c ticket c div G of its home group at launch is what the page's
+    protocol gives when every worker fetches once, in worker order, before any fetches
+    again: under that schedule the two models produce the same visits.  (With T >= P + G
+    every home group holds a ticket for each of its home workers; with fewer tiles a
+    first-round worker of the page's protocol may already steal, and the two models may
+    give a stolen tile to different workers, both valid.)"""
+    rnd = random.Random(300 + seed)
+    P, G = rnd.randint(1, 24), rnd.choice([1, 2, 3, 8])
+    G = min(G, P)
+    T = rnd.randint(P + G, 400)
+    first_round = list(range(P))
+
+    def pick_factory():
+        queue = list(first_round)
+        r = random.Random(seed)
+
+        def pick(live):
+            while queue:
+                c = queue.pop(0)
+                if c in live:
+                    return c
+            return r.choice(live)
+        return pick
+    plain = S.ws_simulate(T, P, G, pick_factory(), layout=layout)
+    implied = S.ws_simulate(T, P, G, pick_factory(), layout=layout, implied_first=True)
+    assert implied == plain
+
+
+@pytest.mark.parametrize("layout", [S.WS_RANGES, S.WS_STRIPED])
+@pytest.mark.parametrize("seed", range(10))
+def test_ws_implied_first_random_interleavings_valid(layout, seed):
+    rnd = random.Random(400 + seed)
+    T, P = rnd.randint(0, 300), rnd.randint(1, 20)
+    G = min(rnd.choice([1, 2, 3, 8]), P)
+    visits = S.ws_simulate(T, P, G, lambda live: rnd.choice(live), layout=layout, implied_first=True)
+    S.check_ws_trace(visits, T, G, layout)
+    for c, v in enumerate(visits):  # each worker's first tile is its launch ticket, when it has one
+        tiles = S.ws_group_tiles(T, G, layout)[c % G]
+        if c // G < len(tiles):
+            assert v[0] == tiles[c // G]
+
+
+@pytest.mark.parametrize("T,P,G", [(0, 4, 4), (1, 8, 4), (3, 20, 8), (9, 12, 5), (30, 30, 8)])
+def test_ws_implied_first_few_tiles_valid(T, P, G):
+    """Fewer tiles than launch tickets: workers whose launch ticket lies past their group's
+    size go straight to stealing, and every tile is still visited once."""
+    for layout in (S.WS_RANGES, S.WS_STRIPED):
+        for seed in range(5):
+            rnd = random.Random(seed)
+            visits = S.ws_simulate(T, P, G, lambda live: rnd.choice(live), layout=layout, implied_first=True)
+            S.check_ws_trace(visits, T, G, layout)
+
+
+def test_ws_implied_first_release_from_start_keeps_the_launch_tile():
+    T, P, G = 120, 16, 4
+    rnd = random.Random(9)
+    visits = S.ws_simulate(T, P, G, lambda live: rnd.choice(live), release_at=lambda step: frozenset({1, 2}),
+                           implied_first=True)
+    S.check_ws_trace(visits, T, G)
+    for c, v in enumerate(visits):
+        if c % G in (1, 2):
+            assert v == S.ws_group_tiles(T, G, S.WS_RANGES)[c % G][c // G: c // G + 1]
+
+
+def test_ws_implied_first_without_the_counter_offset_is_rejected():
+    """Planted mistake: counters standing for tickets from 0 instead of from the number of
+    home workers hand the launch tickets out twice; the validator must reject the trace."""
+    T, P, G = 96, 12, 4
+    st = S.WsState(T, P, G, S.WS_RANGES, implied_first=True)
+    st.offset = [0] * G
+    visits = [[] for _ in range(P)]
+    live = list(range(P))
+    rnd = random.Random(3)
+    while live:
+        c = rnd.choice(live)
+        t = st.fetch(c)
+        if t < 0:
+            live.remove(c)
+        else:
+            visits[c].append(t)
+    with pytest.raises(AssertionError):
+        S.check_ws_trace(visits, T, G)
+
+
 def test_ws_single_group_round_robin_is_interleaved():
     T, P = 37, 5
     order = itertools.cycle(range(P))
