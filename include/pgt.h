@@ -73,9 +73,11 @@ extern "C" {
  *                      steals from the following groups ([WS]); tiles decoded like
  *                      SWIZZLED (linear when group_size == 1).  G = min(ws_groups, P):
  *                      every group has a home worker, as on the page, where the groups
- *                      (XCDs) are far fewer than the workers (CUs).  A worker takes its
- *                      home group's next ticket a few pipeline stages before it needs it;
- *                      the release flag is read before each ticket is taken.
+ *                      (XCDs) are far fewer than the workers (CUs).  Worker p's first
+ *                      tile is ticket p div G of its home group, assigned at launch (a
+ *                      group's counter then hands out tickets from its number of home
+ *                      workers on, and still starts each launch at zero); a worker takes
+ *                      its next home ticket a few pipeline stages before it needs it.
  *   BLOCKED_GROUPED_M: blocked order with the L2-grouping decode, bands of group_size
  *                      tile rows ([PK] "PERSISTENT BLOCKED WITH L2 GROUPING").
  * P is the number of persistent workers (CTAs, or CTA pairs for 2-CTA kernels) and
@@ -200,11 +202,14 @@ int pgt_destroy(pgt_ctx* ctx);
  * XCD" and "Request CU release from the scheduler kernel", which spin on host memory; this
  * is a bounded rework).  Copies n flags (host int32, nonzero = release) into the context's
  * per-group device flags with cudaMemcpyAsync on `stream` — which may differ from the
- * stream of a running GEMM, so a release can land mid-launch.  Before every tile fetch a
- * WORK_STEALING worker reads its home group's flag once (no spinning) and, if it is raised,
- * takes no further tiles; the other workers steal what is left, so the output is complete
- * and identical.  Group 0 is never released (its workers always finish the GEMM).  Flags
- * stay raised until cleared by another call; static modes ignore them.  n in
+ * stream of a running GEMM, so a release can land mid-launch.  A WORK_STEALING worker
+ * reads its home group's flag (no spinning) before each ticket it would take from a counter
+ * (the read is issued one decision ahead, so a raised flag takes effect within a tile) and,
+ * if it is raised, takes no further tiles; the other workers steal what is left, so the
+ * output is complete and identical.  A worker released before launch still runs the one
+ * tile it is assigned at launch.  Group 0 is never released (its workers always finish).  Flags
+ * stay raised until cleared by another call; static modes ignore them.  Until this is first
+ * called on a context, its work-stealing launches do not read the flags at all.  n in
  * [1, max_groups]; pinned host memory keeps the copy asynchronous. */
 int pgt_set_release(pgt_ctx* ctx, const int32_t* h_flags, int n, void* stream);
 

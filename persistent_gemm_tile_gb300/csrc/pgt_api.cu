@@ -111,7 +111,7 @@ int schedule_log_launch(pgt_ctx* ctx, int64_t m_blocks, int64_t n_blocks, int cl
     sp.workers = num_workers;
     sp.counters = ctx->d_counters;
     sp.done = ctx->d_done;
-    sp.release = ctx->d_release;
+    sp.release = ctx->release_armed ? ctx->d_release : nullptr;
     if (sched_mode == PGT_WORK_STEALING && (ctx->flags & PGT_FLAG_HOST_RESET)) {
         if (cudaMemsetAsync(ctx->d_counters, 0, sizeof(int) * kCounterStride * (ctx->max_groups + 1), stream) !=
             cudaSuccess)
@@ -182,6 +182,8 @@ int pgt_destroy(pgt_ctx* ctx) {
 int pgt_set_release(pgt_ctx* ctx, const int32_t* h_flags, int n, void* stream) {
     if (ctx == nullptr || h_flags == nullptr || n < 1 || n > ctx->max_groups) return PGT_ERR_ARG;
     if (cudaSetDevice(ctx->device) != cudaSuccess) return PGT_ERR_CUDA;
+    // from now on work-stealing launches read the flags (until then they skip the reads)
+    ctx->release_armed = true;
     return cuda_status(cudaMemcpyAsync(ctx->d_release, h_flags, sizeof(int32_t) * n, cudaMemcpyHostToDevice,
                                        static_cast<cudaStream_t>(stream)));
 }

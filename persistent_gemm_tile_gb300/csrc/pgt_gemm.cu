@@ -390,7 +390,7 @@ int gemm_launch(pgt_ctx* ctx, const pgt_gemm_desc& d, const pgt_gemm_plan_info& 
     gp.sp.workers = plan.workers;
     gp.sp.counters = ctx->d_counters;
     gp.sp.done = ctx->d_done;
-    gp.sp.release = ctx->d_release;
+    gp.sp.release = ctx->release_armed ? ctx->d_release : nullptr;  // no reads until release is used
     gp.err = ctx->d_err;
     gp.sfa_rows = 0;
     gp.sfb_rows = 0;

@@ -167,12 +167,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int worker = blockIdx.x / CS;
 
     // The producer thread of the worker (the leader CTA's thread 0) runs the scheduler.
-    // Work stealing takes the first ticket here, so its round trip overlaps the set-up below.
+    // Work stealing starts reading its release flag here, so the read overlaps the set-up.
     Scheduler sch;
-    if (threadIdx.x == 0 && leader) {
-        sch.init(gp.sp, worker);
-        sch.take_ahead();
-    }
+    if (threadIdx.x == 0 && leader) sch.init(gp.sp, worker);
 
     const uint32_t bar0 = base + L::BAR_OFF;
     auto full = [&](int s) { return bar0 + 8u * s; };

@@ -17,6 +17,7 @@ struct pgt_ctx {
     int* d_err;       // device error word: code, role, block, site
     int* d_release;   // work-stealing release flags, one int per group (two 128-byte lines)
     void* d_block;    // the single allocation holding the three above
+    bool release_armed;  // pgt_set_release was called: kernels read the flags (else they skip them)
 };
 
 namespace pgt {

@@ -82,6 +82,7 @@ extern "C" int pgt_gemm_noalloc(const void* A, const void* B, void* C, int64_t M
     c.d_err = d_err != nullptr ? d_err : c.d_done + pgt::kCounterStride;
     c.d_release = nullptr;
     c.d_block = nullptr;
+    c.release_armed = false;
 
     pgt_gemm_desc in = {};
     in.M = M;

@@ -79,27 +79,45 @@ __device__ __forceinline__ void decode_tile(const SchedParams& p, int t, int& m,
     }
 }
 
-// Range of counter group g: [g*T/G, (g+1)*T/G).
-__device__ __forceinline__ int ws_group_start(int g, int T, int G) {
-    return static_cast<int>((static_cast<long long>(g) * T) / G);
-}
-
-// Tiles owned by counter group g, and the tile its ticket j stands for.  Ranges: the
-// contiguous [g*T/G, (g+1)*T/G) (one region per group, as the per-XCD counters of the
-// tritonBLAS PR).  Striped: g, g+G, g+2G, ... (every group on the same front of the
-// decode order: one shared L2).
-__device__ __forceinline__ int ws_group_size(int g, int T, int G, int layout) {
-    if (layout == 1) return T / G + (g < T % G ? 1 : 0);
-    return ws_group_start(g + 1, T, G) - ws_group_start(g, T, G);
-}
-
-__device__ __forceinline__ int ws_group_tile(int g, int ticket, int T, int G, int layout) {
-    if (layout == 1) return ticket * G + g;
-    return ws_group_start(g, T, G) + ticket;
-}
+// Tiles owned by work-stealing counter group g of G, with T tiles in all, and the tile its
+// ticket j stands for.  Ranges: the contiguous [floor(g*T/G), floor((g+1)*T/G)) (one region
+// per group, as the per-XCD counters of the tritonBLAS PR).  Striped: g, g+G, g+2G, ...
+// (every group on the same front of the decode order: one shared L2).  With q = T div G and
+// r = T mod G precomputed, floor(g*T/G) = g*q + floor(g*r/G) exactly, so a lookup costs one
+// small 32-bit division instead of a 64-bit one (g*T can exceed 32 bits).
+struct WsGroups {
+    int G, layout, q, r;
+    __device__ __forceinline__ void init(int T, int groups, int lay) {
+        G = groups;
+        layout = lay;
+        q = T / groups;
+        r = T - q * groups;
+    }
+    __device__ __forceinline__ int start(int g) const { return g * q + (g * r) / G; }
+    __device__ __forceinline__ int size(int g) const {
+        if (layout == 1) return q + (g < r ? 1 : 0);
+        return start(g + 1) - start(g);
+    }
+    __device__ __forceinline__ int tile(int g, int ticket) const {
+        if (layout == 1) return ticket * G + g;
+        return start(g) + ticket;
+    }
+};
 
 // Per-worker scheduler.  Static modes are pure functions of (worker, iteration); work
 // stealing draws tickets from the counters.
+//
+// Work stealing hides the protocol's round trips from the tile pipeline:
+//  * a worker's first ticket of its home group is implied: worker w, homed on g = w mod G,
+//    takes ticket w div G at launch, and the counter of g hands out tickets from n_g (the
+//    number of workers homed on g) on, so counters still start every launch at zero;
+//  * the next home ticket is taken a few pipeline stages before it is needed (take_ahead),
+//    together with reads of the following groups' counters for a steal scan;
+//  * the home group's release flag is read one decision ahead and its value used at the
+//    next one, so no decision waits for it.  A worker released before launch still runs
+//    its implied first tile; a release raised later lands within a tile.
+// Every tile is still handed out exactly once, and a worker's tickets in a group still
+// increase (the validator's invariants).
 struct Scheduler {
     SchedParams p;
     int next;    // static: next tile id
@@ -107,9 +125,13 @@ struct Scheduler {
     int stride;  // static: step between tile ids
     int home;    // work stealing: home group
     int cursor;  // work stealing: groups found exhausted, counted from home
-    int ahead;   // work stealing: a home-group ticket taken before the fetch that uses it
+    int first;   // work stealing: the implied first ticket of the home group (-1 once used)
+    int ahead;   // work stealing: a home-group counter value taken before the fetch that uses it
     bool has_ahead;
     bool stopped;  // work stealing: the home group's release flag was seen
+    int rel;       // work stealing: the release flag as last read (used at the next decision)
+    WsGroups wg;   // work stealing: the groups' tiles
+    int wq, wr;    // work stealing: P div G, P mod G (workers homed on each group)
     static constexpr int kScan = 8;  // counters read at once by a steal scan
     int scan[kScan];                 // work stealing: the following groups' counters, read with `ahead`
 
@@ -117,9 +139,11 @@ struct Scheduler {
         p = params;
         home = 0;
         cursor = 0;
+        first = -1;
         ahead = 0;
         has_ahead = false;
         stopped = false;
+        rel = 0;
         if (p.mode == kBlocked || p.mode == kBlockedGroupedM) {
             const int B = (p.tiles + p.workers - 1) / p.workers;
             const long long s = static_cast<long long>(worker) * B;
@@ -127,15 +151,24 @@ struct Scheduler {
             end = static_cast<int>(s + B < p.tiles ? s + B : p.tiles);
             stride = 1;
         } else if (p.mode == kWorkStealing) {
+            wg.init(p.tiles, p.ws_groups, p.ws_layout);
+            wq = p.workers / p.ws_groups;
+            wr = p.workers - wq * p.ws_groups;
             home = worker % p.ws_groups;
+            first = worker / p.ws_groups;
             next = end = 0;
             stride = 0;
+            read_release();
         } else {
             next = worker;
             end = p.tiles;
             stride = p.workers;
         }
     }
+
+    // Work stealing: workers homed on group g (G <= P, so at least one): the implied tickets
+    // 0 .. n_g - 1 of g belong to them, and the counter's value c stands for ticket c + n_g.
+    __device__ __forceinline__ int homed(int g) const { return wq + (g < wr ? 1 : 0); }
 
     // Work stealing: the counter of the group `offset` places after home (0 past the last).
     __device__ __forceinline__ int read_counter(int offset) const {
@@ -145,21 +178,21 @@ struct Scheduler {
         return *reinterpret_cast<const volatile int*>(p.counters + g * kCounterStride);
     }
 
-    // Work stealing: cooperative release.  A raised flag of the home group (never group 0,
-    // whose workers finish whatever is left) stops this worker before its next ticket.
-    __device__ __forceinline__ bool released() const {
-        return p.release != nullptr && home != 0 && *reinterpret_cast<const volatile int*>(p.release + home) != 0;
+    // Work stealing: cooperative release.  Start reading the home group's flag (never group
+    // 0's: its workers finish whatever is left); the value is used by the next decision.
+    __device__ __forceinline__ void read_release() {
+        rel = (p.release != nullptr && home != 0) ? *reinterpret_cast<const volatile int*>(p.release + home) : 0;
     }
 
     // Work stealing: take the home group's next ticket now, so that the atomic's round trip
-    // overlaps other work (the producer calls this a few stages before a tile's last load,
-    // and for the first tile at kernel entry); the next fetch consumes it.  The release flag
-    // is read before the ticket is taken, and a ticket taken is always used, so every tile is
-    // still handed out exactly once.  Once the home group is exhausted (stealing), tickets
-    // are taken by fetch itself.  The result register is only read by that fetch.
+    // overlaps other work (the producer calls this a few stages before a tile's last load);
+    // the next fetch consumes it.  A raised release flag stops the worker instead, and a
+    // ticket taken is always used, so every tile is still handed out exactly once.  Once the
+    // home group is exhausted (stealing), tickets are taken by fetch itself.  The result
+    // registers are only read by that fetch.
     __device__ __forceinline__ void take_ahead() {
-        if (p.mode != kWorkStealing || cursor != 0 || has_ahead || stopped) return;
-        if (released()) {
+        if (p.mode != kWorkStealing || cursor != 0 || has_ahead || stopped || first >= 0) return;
+        if (rel != 0) {
             stopped = true;
             return;
         }
@@ -169,38 +202,50 @@ struct Scheduler {
         // (issued together with the atomic, so the fetch saves a round trip)
 #pragma unroll
         for (int j = 0; j < kScan; ++j) scan[j] = read_counter(1 + j);
+        read_release();
     }
 
     // Next tile id, or -1 when this worker is done.
     __device__ __forceinline__ int fetch() {
         if (p.mode == kWorkStealing) {
             // home group first; once it is exhausted, steal from the following groups.  Counters
-            // only grow during a launch, so a group whose counter already reads >= its size is
+            // only grow during a launch, so a group whose counter already reads at its size is
             // exhausted: the steal scan reads up to kScan counters at once (independent loads)
             // and takes an atomic ticket only where one may be left.
+            const int size_home = wg.size(home);
             bool pre = false;  // the first steal scan may use the counters read ahead
-            if (has_ahead) {
-                has_ahead = false;
-                if (ahead < ws_group_size(home, p.tiles, p.ws_groups, p.ws_layout))
-                    return ws_group_tile(home, ahead, p.tiles, p.ws_groups, p.ws_layout);
-                cursor = 1;
-                pre = true;
-            } else {
-                if (stopped || released()) {
+            if (first >= 0) {
+                const int t = first;
+                first = -1;
+                if (t < size_home) return wg.tile(home, t);
+                cursor = 1;  // an implied ticket past the group's size: every ticket of it is taken
+                if (rel != 0) {  // and stealing takes atomics, which a release forbids
                     stopped = true;
                     return -1;
                 }
+                read_release();
+            } else if (has_ahead) {
+                has_ahead = false;
+                const int ticket = ahead + homed(home);
+                if (ticket < size_home) return wg.tile(home, ticket);
+                cursor = 1;
+                pre = true;
+            } else {
+                if (stopped || rel != 0) {
+                    stopped = true;
+                    return -1;
+                }
+                read_release();
                 if (cursor == 0) {
-                    const int size = ws_group_size(home, p.tiles, p.ws_groups, p.ws_layout);
-                    const int ticket = atomicAdd(p.counters + home * kCounterStride, 1);
-                    if (ticket < size) return ws_group_tile(home, ticket, p.tiles, p.ws_groups, p.ws_layout);
+                    const int ticket = atomicAdd(p.counters + home * kCounterStride, 1) + homed(home);
+                    if (ticket < size_home) return wg.tile(home, ticket);
                     cursor = 1;
                 }
             }
             while (cursor < p.ws_groups) {
-                // Counters only grow during a launch: a value read earlier that is already at
-                // the group's size means exhausted; one below it is only a hint (the atomic
-                // decides), so reads taken ahead serve as well as fresh ones.
+                // A value read earlier that already reaches the group's size means exhausted;
+                // one below it is only a hint (the atomic decides), so reads taken ahead serve
+                // as well as fresh ones.
                 int seen[kScan];
 #pragma unroll
                 for (int j = 0; j < kScan; ++j) seen[j] = pre ? scan[j] : read_counter(cursor + j);
@@ -211,10 +256,11 @@ struct Scheduler {
                     if (cursor >= p.ws_groups) break;
                     int g = home + cursor;
                     while (g >= p.ws_groups) g -= p.ws_groups;
-                    const int size = ws_group_size(g, p.tiles, p.ws_groups, p.ws_layout);
-                    if (seen[j] < size) {
-                        const int ticket = atomicAdd(p.counters + g * kCounterStride, 1);
-                        if (ticket < size) return ws_group_tile(g, ticket, p.tiles, p.ws_groups, p.ws_layout);
+                    const int size = wg.size(g);
+                    const int n = homed(g);
+                    if (seen[j] + n < size) {
+                        const int ticket = atomicAdd(p.counters + g * kCounterStride, 1) + n;
+                        if (ticket < size) return wg.tile(g, ticket);
                     }
                     ++cursor;
                 }

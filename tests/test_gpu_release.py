@@ -22,6 +22,13 @@ def ctx():
     c.close()
 
 
+def implied_first_tile(T, G, layout, w):
+    """The tile a work-stealing worker is given at launch: ticket w div G of its home group
+    w mod G (none when the group has fewer tickets)."""
+    tiles = S.ws_group_tiles(T, G, layout)[w % G]
+    return tiles[w // G: w // G + 1]
+
+
 def test_schedule_log_release_from_start(ctx):
     G, P = 4, 64
     ctx.set_release([1, 1, 1, 0])  # group 0's flag is ignored
@@ -32,8 +39,9 @@ def test_schedule_log_release_from_start(ctx):
     torch.cuda.synchronize()
     visits, _ = tb.read()
     S.check_ws_trace([[t for (t, _, _, _) in v] for v in visits], grid.tiles, G)
-    assert all(len(v) == 0 for c, v in enumerate(visits) if c % G in (1, 2))
-    assert sum(len(v) for c, v in enumerate(visits) if c % G in (0, 3)) == grid.tiles
+    for c, v in enumerate(visits):
+        if c % G in (1, 2):  # released before launch: only the tile assigned at launch
+            assert [t for (t, _, _, _) in v] == implied_first_tile(grid.tiles, G, S.WS_RANGES, c), c
 
 
 @pytest.mark.parametrize("cfg", [pgt.CFG_1CTA_128x256, pgt.CFG_2CTA_256x256])
@@ -57,7 +65,9 @@ def test_gemm_release_from_start_same_bits(ctx, cfg):
     wv = [visits[w * cs] for w in range(plan["workers"])]
     assert plan["ws_groups"] == 8
     S.check_ws_trace([[t for (t, _, _, _) in v] for v in wv], plan["tiles"], 8)
-    assert all(len(v) == 0 for w, v in enumerate(wv) if w % 8 != 0)
+    for w, v in enumerate(wv):
+        if w % 8 != 0:  # released before launch: only the tile assigned at launch
+            assert [t for (t, _, _, _) in v] == implied_first_tile(plan["tiles"], 8, S.WS_RANGES, w), w
 
 
 def test_gemm_release_mid_launch_from_another_stream(ctx):
@@ -71,6 +81,8 @@ def test_gemm_release_mid_launch_from_another_stream(ctx):
     plan = ctx.gemm_plan(desc)
     tb = pgt.TraceBuffers(plan["ctas"], plan["tiles"])
     C = torch.full((M, N), -1, dtype=torch.int16, device="cuda")
+    ctx.set_release(np.zeros(8, np.int32))  # arm the flags: launches read them from now on
+    torch.cuda.synchronize()
     side = torch.cuda.Stream()
     flags = torch.ones(8, dtype=torch.int32).pin_memory()
     ctx.gemm_ex(desc, dA, dB, C, trace=tb.struct)  # current stream
