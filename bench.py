@@ -41,9 +41,12 @@ L2_NOTE = "inputs larger than L2: A+B+C = 384 MiB per GEMM > 129 MB L2; add x+y+
 GEMM_SOURCES = ["csrc/pgt_gemm_kernel.cuh", "csrc/pgt_device.cuh", "csrc/pgt_sched.cuh"]
 ADD_SOURCES = ["csrc/pgt_add.cu", "csrc/pgt_device.cuh", "csrc/pgt_sched.cuh"]
 PROFILED_TRAFFIC = {
-    "gemm_bf16_2cta_256x256": (8.73577472e+08 + 1.27464704e+08, GEMM_SOURCES, "230ce9d380f60ad1"),
-    "add_page_32x16_blocked": (5.3693696e+08 + 2.32903936e+08, ADD_SOURCES, "71df49dcd8988376"),
-    "add_page_32x16_interleaved": (5.6740352e+08 + 2.38276352e+08, ADD_SOURCES, "71df49dcd8988376"),
+    "gemm_bf16_2cta_256x256": (8.70600960e+08 + 1.27245056e+08, GEMM_SOURCES, "35b091e2cad17125"),
+    "gemm_mxfp8_2cta_256x256": (2.48183040e+08 + 1.16106240e+08, GEMM_SOURCES, "35b091e2cad17125"),
+    "add_wide_8x1024_blocked": (5.36980992e+08 + 2.31485952e+08, ADD_SOURCES, "a63d73d6e750a2c1"),
+    "add_wide_8x1024_interleaved": (5.36940544e+08 + 2.31300864e+08, ADD_SOURCES, "a63d73d6e750a2c1"),
+    "add_page_32x16_blocked": (5.36929536e+08 + 2.32817664e+08, ADD_SOURCES, "a63d73d6e750a2c1"),
+    "add_page_32x16_interleaved": (5.75323904e+08 + 2.37948160e+08, ADD_SOURCES, "a63d73d6e750a2c1"),
 }
 
 
@@ -82,6 +85,9 @@ def parse():
                                                          "e.g. 32x16 (the page's tile)")
     ap.add_argument("--add-sched", default="blocked", choices=["blocked", "interleaved"],
                     help="scheduler of the --kernel add headline")
+    ap.add_argument("--cublas", action="store_true",
+                    help="with --kernel mxfp8: also time cuBLAS's MXFP8 GEMM on the same operands after the "
+                         "timed loop (for profiling the two side by side)")
     ap.add_argument("--no-ragged", action="store_true",
                     help="skip the ragged-tail GEMM set (timed per scheduler, with tail idle from traces)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
@@ -507,9 +513,19 @@ def run_mx_headline(args, world, rank, local, pg, torch, pgt, ctx, device, peaks
            "config": {"workload": f"MXFP8 {M}^3 seed 4, swizzled group 16", "kernel_cfg": plan["kernel_cfg"],
                       "tile": f"{plan['bm'] * plan['cluster_size']}x{plan['bn']}", "l2": L2_NOTE},
            "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                        "frac": achieved / fp8_peak, "traffic": None,
+                        "frac": achieved / fp8_peak,
+                        "traffic": profiled_traffic("gemm_mxfp8_2cta_256x256") if plan["kernel_cfg"] == 4 else None,
                         "peak_kind": f"2 x bf16 burst ({peaks['source']})"},
            "gpu_launches": 2 * args.steps, "clocks": clk}
+    if args.cublas:
+        lib_launch, lib_out = cublas_mxfp8(torch, qa, sa, qb, sb, device)
+        if lib_launch is None:
+            out["vs_cublas"] = {"unavailable": lib_out}
+        else:
+            _, lper = time_launches(torch, lib_launch, max(3, args.steps), args.warmup)
+            lms = float(np.median(lper))
+            out["vs_cublas"] = {"cublas_tflops": FLOP / (lms * 1e-3) / 1e12, "ours_tflops": achieved,
+                                "bit_identical_outputs": bool(torch.equal(dC.view(torch.bfloat16), lib_out))}
     if rank == 0:
         print(json.dumps(out), flush=True)
     ctx.close()
