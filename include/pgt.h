@@ -68,8 +68,9 @@ extern "C" {
  *   SWIZZLED:          interleaved waves (tile = P*w + p, [TS]) with the group_size
  *                      column-group decode and 2-CTA pairing ([TS]).
  *   WORK_STEALING:     tiles handed out through per-group atomic counters; G counters,
- *                      group g owns tiles [g*T/G, (g+1)*T/G) (or, with PGT_WS_STRIPED,
- *                      the tiles t = g mod G); a worker starts at group (p mod G) and
+ *                      worker p homed on group p mod G, each group owning a share of the
+ *                      tiles in proportion to its home workers (PGT_WS_RANGES /
+ *                      PGT_WS_STRIPED below); a worker starts at its home group and
  *                      steals from the following groups ([WS]); tiles decoded like
  *                      SWIZZLED (linear when group_size == 1).  G = min(ws_groups, P):
  *                      every group has a home worker, as on the page, where the groups
@@ -78,6 +79,8 @@ extern "C" {
  *                      group's counter then hands out tickets from its number of home
  *                      workers on, and still starts each launch at zero); a worker takes
  *                      its next home ticket a few pipeline stages before it needs it.
+ *                      With T <= P every ticket is assigned at launch and no counter is
+ *                      touched.  P at most 65535 (PGT_ERR_ARG otherwise).
  *   BLOCKED_GROUPED_M: blocked order with the L2-grouping decode, bands of group_size
  *                      tile rows ([PK] "PERSISTENT BLOCKED WITH L2 GROUPING").
  * P is the number of persistent workers (CTAs, or CTA pairs for 2-CTA kernels) and
@@ -127,12 +130,17 @@ extern "C" {
 #define PGT_VISIT_FIELDS 4 /* tile_id, m_idx, n_idx, smid */
 
 /* Which tiles each work-stealing counter group owns (ticket j of group g is its j-th tile).
- *   RANGES:  the contiguous range [g*T/G, (g+1)*T/G) ([WS]: one counter per XCD, each XCD
- *            with its own L2 working on its own region).
- *   STRIPED: tiles g, g+G, g+2G, ...: every group advances along the same front of the
- *            decode order, so the tiles in flight are the ones a static schedule would run
- *            at that time.  This suits a GPU whose L2 all SMs share.  Counters, homes,
- *            stealing, release and reset are the same. */
+ * n_g = P div G + (g < P mod G) workers are homed on group g, S_g = n_0 + ... + n_{g-1}.
+ *   RANGES:  the contiguous range [floor(T*S_g/P), floor(T*S_{g+1}/P)), a share in
+ *            proportion to n_g; [g*T/G, (g+1)*T/G) when G divides P ([WS]: one counter per
+ *            XCD, the XCDs holding equal numbers of CUs, each XCD with its own L2 working on
+ *            its own region).
+ *   STRIPED: the tiles t with (t mod P) mod G == g, in increasing order: those the workers
+ *            homed on g would visit in the INTERLEAVED order (g, g+G, g+2G, ... when G
+ *            divides P).  Every group advances along the same front of the decode order,
+ *            so the tiles in flight are the ones a static schedule would run at that time.
+ *            This suits a GPU whose L2 all SMs share.  Counters, homes, stealing, release
+ *            and reset are the same. */
 #define PGT_WS_RANGES 0
 #define PGT_WS_STRIPED 1
 
@@ -347,7 +355,8 @@ int pgt_multi_loop(pgt_ctx* ctx, const pgt_scale_space* spaces, int n_spaces, in
  * single-thread worker per block; num_workers >= 1, and for PGT_LAUNCH_CONTROL exactly the
  * tile count (one worker per tile; cancelled workers record nothing).  Work stealing uses
  * the context's counters and release flags like the GEMM, with ws_layout a PGT_WS_* and
- * min(ws_groups, num_workers) counter groups. */
+ * min(ws_groups, num_workers) counter groups (num_workers at most 65535, PGT_ERR_ARG
+ * otherwise). */
 int pgt_schedule_log(pgt_ctx* ctx, int64_t m_blocks, int64_t n_blocks, int cluster_size,
                      int sched_mode, int group_size, int ws_groups, int ws_layout, int num_workers,
                      const pgt_trace* trace, void* stream);

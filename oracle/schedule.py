@@ -28,9 +28,12 @@ Decodes:
 
 Work stealing (tritonBLAS "Work Stealing Scheduler Kernel": per-XCD int32 tile counters
 indexed by ``pid % NUM_XCDS``, reset before each launch).  The fetch body is not on that
-page; the reading adopted here: ``G_ws`` counters; group ``g`` owns the contiguous tile
-range ``[floor(g*T/G_ws), floor((g+1)*T/G_ws))``; worker ``c`` starts at its home group
-``c mod G_ws``; a fetch is ``ticket = atomic_add(counter[g], 1)`` and succeeds when
+page; the reading adopted here: ``G_ws`` counters; worker ``c`` of ``P`` has the home group
+``c mod G_ws``, so ``n_g`` workers are homed on group ``g``; group ``g`` owns the contiguous
+tile range ``[floor(T*S_g/P), floor(T*S_{g+1}/P))`` with ``S_g = n_0 + ... + n_{g-1}``, a share
+of the tiles in proportion to its home workers (on the page's GPU every XCD holds the same
+number of CUs, so this is the even split ``[floor(g*T/G_ws), floor((g+1)*T/G_ws))`` whenever
+``G_ws`` divides ``P``); a fetch is ``ticket = atomic_add(counter[g], 1)`` and succeeds when
 ``ticket < size_g`` (tile ``start_g + ticket``); an exhausted group sends the worker on to
 ``g+1, g+2, ...`` (mod ``G_ws``) and it stops once it has found all ``G_ws`` groups
 exhausted.  Stolen tiles are decoded with the swizzled decode (linear when ``G <= 1``).
@@ -39,10 +42,12 @@ are fixed.
 
 Tile ownership ``layout``: ``WS_RANGES`` is the reading above (the page's per-XCD
 counters, each over its own contiguous range, so each XCD's L2 sees one region).
-``WS_STRIPED`` is a variant for a GPU whose L2 all groups share: group ``g`` owns the
-tiles ``t`` with ``t mod G_ws == g``, ticket ``j`` being tile ``j*G_ws + g``, so the
-groups advance together along the decode order.  Counters, homes, stealing, release and
-reset are unchanged.
+``WS_STRIPED`` is a variant for a GPU whose L2 all groups share: tile ``t`` belongs to the
+home group of worker ``t mod P``, i.e. group ``(t mod P) mod G_ws``, in increasing order (the
+tiles that worker would visit in the interleaved order), so the groups advance together
+along the decode order; whenever ``G_ws`` divides ``P`` that is ``t mod G_ws == g``, ticket
+``j`` being tile ``j*G_ws + g``.  Counters, homes, stealing, release and reset are
+unchanged.
 
 First tickets assigned at launch (``implied_first``): the page's loop takes every ticket
 from a counter; the GB300 build assigns worker ``c``'s first ticket without an atomic:
@@ -155,18 +160,27 @@ def static_schedule(mode: int, grid: Grid, P: int, G: int) -> list[list[tuple[in
 
 
 # ------------------------------------------------------------------------ work stealing
-def ws_partition(T: int, groups: int) -> list[tuple[int, int]]:
-    """(start, size) of each counter group's contiguous tile range."""
-    bounds = [(g * T) // groups for g in range(groups + 1)]
+def ws_homed(P: int, groups: int) -> list[int]:
+    """Workers homed on each counter group (worker c's home is c mod groups)."""
+    return [sum(1 for c in range(P) if c % groups == g) for g in range(groups)]
+
+
+def ws_partition(T: int, groups: int, P: int) -> list[tuple[int, int]]:
+    """(start, size) of each counter group's contiguous tile range: group g's share of the T
+    tiles is in proportion to the workers homed on it."""
+    S = [0]
+    for n in ws_homed(P, groups):
+        S.append(S[-1] + n)
+    bounds = [(T * s) // P for s in S]
     return [(bounds[g], bounds[g + 1] - bounds[g]) for g in range(groups)]
 
 
-def ws_group_tiles(T: int, groups: int, layout: int = WS_RANGES) -> list[list[int]]:
+def ws_group_tiles(T: int, groups: int, layout: int, P: int) -> list[list[int]]:
     """Each counter group's tiles in ticket order (ticket j is the list's j-th tile)."""
     if layout == WS_RANGES:
-        return [list(range(s, s + n)) for s, n in ws_partition(T, groups)]
+        return [list(range(s, s + n)) for s, n in ws_partition(T, groups, P)]
     if layout == WS_STRIPED:
-        return [list(range(g, T, groups)) for g in range(groups)]
+        return [[t for t in range(T) if (t % P) % groups == g] for g in range(groups)]
     raise ValueError(f"unknown tile layout {layout}")
 
 
@@ -176,14 +190,14 @@ class WsState:
 
     def __init__(self, T: int, P: int, groups: int, layout: int = WS_RANGES, implied_first: bool = False):
         self.T, self.P, self.groups = T, P, groups
-        self.tiles = ws_group_tiles(T, groups, layout)
+        self.tiles = ws_group_tiles(T, groups, layout, P)
         self.counter = [0] * groups
         self.cursor = [0] * P  # groups already found exhausted, counted from home
         self.done = [False] * P
         self.implied_first = implied_first
         self.started = [False] * P
         # tickets assigned at launch per group: one per worker homed there
-        self.offset = [sum(1 for c in range(P) if c % groups == g) if implied_first else 0 for g in range(groups)]
+        self.offset = ws_homed(P, groups) if implied_first else [0] * groups
 
     def fetch(self, c: int, released=frozenset()) -> int:
         """One fetch by worker c; returns a tile id or -1 once every group is exhausted.
@@ -239,12 +253,13 @@ def check_ws_trace(visits: list[list[int]], T: int, groups: int, layout: int = W
 
     Raises AssertionError unless: every tile in [0, T) is visited exactly once; inside each
     counter group a worker's tickets increase; and a worker's groups follow its cyclic
-    order from home (home, home+1, ...), never going back to a group it left.
+    order from home (home, home+1, ...), never going back to a group it left.  The worker
+    count P, on which the groups' tiles depend, is the number of lists.
     """
     flat = sorted(t for v in visits for t in v)
     assert flat == list(range(T)), "work-stealing visits are not a permutation of the tiles"
     owner, ticket = {}, {}
-    for g, tiles in enumerate(ws_group_tiles(T, groups, layout)):
+    for g, tiles in enumerate(ws_group_tiles(T, groups, layout, len(visits))):
         for j, t in enumerate(tiles):
             owner[t], ticket[t] = g, j
     for c, v in enumerate(visits):

@@ -94,6 +94,7 @@ int schedule_log_launch(pgt_ctx* ctx, int64_t m_blocks, int64_t n_blocks, int cl
     if (m_blocks >= ((int64_t)1 << 31) || n_blocks >= ((int64_t)1 << 31) || tiles >= ((int64_t)1 << 31))
         return PGT_ERR_ARG;
     if (sched_mode == PGT_LAUNCH_CONTROL && num_workers != tiles) return PGT_ERR_ARG;  // one per tile
+    if (sched_mode == PGT_WORK_STEALING && num_workers > kMaxWsWorkers) return PGT_ERR_ARG;
     SchedParams sp;
     sp.tiles = (int)tiles;
     sp.m_tiles = (int)m_tiles;

@@ -324,6 +324,7 @@ int gemm_plan(const pgt_ctx* ctx, const pgt_gemm_desc* in, pgt_gemm_desc* d, pgt
         if (workers < 1) workers = 1;
     }
     if (workers * s.cs >= lim) return PGT_ERR_ARG;
+    if (d->sched_mode == PGT_WORK_STEALING && workers > kMaxWsWorkers) return PGT_ERR_ARG;
     // every counter group gets a home worker (a group without one would only be stolen from)
     if (d->ws_groups > workers) d->ws_groups = (int32_t)workers;
     p->kernel_cfg = d->kernel_cfg;

@@ -23,6 +23,7 @@ struct pgt_ctx {
 namespace pgt {
 
 constexpr int kMaxGroups = 64;
+constexpr int kMaxWsWorkers = 65535;  // work stealing's 32-bit group arithmetic (pgt_sched.cuh)
 
 // Status from a CUDA runtime result.
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? PGT_OK : PGT_ERR_CUDA; }

@@ -79,27 +79,45 @@ __device__ __forceinline__ void decode_tile(const SchedParams& p, int t, int& m,
     }
 }
 
-// Tiles owned by work-stealing counter group g of G, with T tiles in all, and the tile its
-// ticket j stands for.  Ranges: the contiguous [floor(g*T/G), floor((g+1)*T/G)) (one region
-// per group, as the per-XCD counters of the tritonBLAS PR).  Striped: g, g+G, g+2G, ...
-// (every group on the same front of the decode order: one shared L2).  With q = T div G and
-// r = T mod G precomputed, floor(g*T/G) = g*q + floor(g*r/G) exactly, so a lookup costs one
-// small 32-bit division instead of a 64-bit one (g*T can exceed 32 bits).
+// Work-stealing counter groups.  Worker c of P is homed on group c mod G, so n_g = P div G +
+// (g < P mod G) workers are homed on g and S_g = g (P div G) + min(g, P mod G) on the groups
+// before it.  Group g owns a share of the T tiles in proportion to n_g (with P a multiple of
+// G, as on the tritonBLAS PR's GPU with its equal XCDs, the even split):
+//   ranges:  the contiguous [floor(T S_g / P), floor(T S_{g+1} / P)), ticket j = start + j
+//            (one region per group, as the per-XCD counters);
+//   striped: the tiles t with (t mod P) mod G = g in increasing order, i.e. those the
+//            workers homed on g would visit in the interleaved order (every group on the
+//            same front of the decode order: one shared L2); ticket j is
+//            (j div n_g) P + g + (j mod n_g) G.
+// With T = a P + b, floor(T S / P) = a S + floor(b S / P), and b S < P^2 fits 32 unsigned
+// bits for P <= 65535 (the host's limit), so a lookup costs one 32-bit division.  (Host
+// callable too, for a test against the oracle.)
 struct WsGroups {
-    int G, layout, q, r;
-    __device__ __forceinline__ void init(int T, int groups, int lay) {
+    int G, layout, P, a, b, wq, wr;
+    __host__ __device__ __forceinline__ void init(int T, int workers, int groups, int lay) {
         G = groups;
         layout = lay;
-        q = T / groups;
-        r = T - q * groups;
+        P = workers;
+        a = T / workers;
+        b = T - a * workers;
+        wq = workers / groups;
+        wr = workers - wq * groups;
     }
-    __device__ __forceinline__ int start(int g) const { return g * q + (g * r) / G; }
-    __device__ __forceinline__ int size(int g) const {
-        if (layout == 1) return q + (g < r ? 1 : 0);
+    __host__ __device__ __forceinline__ int homed(int g) const { return wq + (g < wr ? 1 : 0); }
+    __host__ __device__ __forceinline__ int start(int g) const {
+        const unsigned s = (unsigned)(g * wq + (g < wr ? g : wr));
+        return (int)(s * (unsigned)a + s * (unsigned)b / (unsigned)P);
+    }
+    __host__ __device__ __forceinline__ int size(int g) const {
+        if (layout == 1) return a * homed(g) + (b > g ? (b - g - 1) / G + 1 : 0);
         return start(g + 1) - start(g);
     }
-    __device__ __forceinline__ int tile(int g, int ticket) const {
-        if (layout == 1) return ticket * G + g;
+    __host__ __device__ __forceinline__ int tile(int g, int ticket) const {
+        if (layout == 1) {
+            const int n = homed(g);
+            const int round = ticket / n;
+            return round * P + g + (ticket - round * n) * G;
+        }
         return start(g) + ticket;
     }
 };
@@ -115,7 +133,9 @@ struct WsGroups {
 //    together with reads of the following groups' counters for a steal scan;
 //  * the home group's release flag is read one decision ahead and its value used at the
 //    next one, so no decision waits for it.  A worker released before launch still runs
-//    its implied first tile; a release raised later lands within a tile.
+//    its implied first tile; a release raised later lands within a tile;
+//  * with no more tiles than workers (T <= P) every ticket of every group is implied, so a
+//    worker runs its launch tile, if it has one, and stops without touching a counter.
 // Every tile is still handed out exactly once, and a worker's tickets in a group still
 // increase (the validator's invariants).
 struct Scheduler {
@@ -131,7 +151,7 @@ struct Scheduler {
     bool stopped;  // work stealing: the home group's release flag was seen
     int rel;       // work stealing: the release flag as last read (used at the next decision)
     WsGroups wg;   // work stealing: the groups' tiles
-    int wq, wr;    // work stealing: P div G, P mod G (workers homed on each group)
+    bool solo;     // work stealing: T <= P, every ticket implied (no counter is touched)
     static constexpr int kScan = 8;  // counters read at once by a steal scan
     int scan[kScan];                 // work stealing: the following groups' counters, read with `ahead`
 
@@ -144,6 +164,7 @@ struct Scheduler {
         has_ahead = false;
         stopped = false;
         rel = 0;
+        solo = false;
         if (p.mode == kBlocked || p.mode == kBlockedGroupedM) {
             const int B = (p.tiles + p.workers - 1) / p.workers;
             const long long s = static_cast<long long>(worker) * B;
@@ -151,9 +172,8 @@ struct Scheduler {
             end = static_cast<int>(s + B < p.tiles ? s + B : p.tiles);
             stride = 1;
         } else if (p.mode == kWorkStealing) {
-            wg.init(p.tiles, p.ws_groups, p.ws_layout);
-            wq = p.workers / p.ws_groups;
-            wr = p.workers - wq * p.ws_groups;
+            wg.init(p.tiles, p.workers, p.ws_groups, p.ws_layout);
+            solo = p.tiles <= p.workers;
             home = worker % p.ws_groups;
             first = worker / p.ws_groups;
             next = end = 0;
@@ -168,7 +188,7 @@ struct Scheduler {
 
     // Work stealing: workers homed on group g (G <= P, so at least one): the implied tickets
     // 0 .. n_g - 1 of g belong to them, and the counter's value c stands for ticket c + n_g.
-    __device__ __forceinline__ int homed(int g) const { return wq + (g < wr ? 1 : 0); }
+    __device__ __forceinline__ int homed(int g) const { return wg.homed(g); }
 
     // Work stealing: the counter of the group `offset` places after home (0 past the last).
     __device__ __forceinline__ int read_counter(int offset) const {
@@ -191,7 +211,7 @@ struct Scheduler {
     // home group is exhausted (stealing), tickets are taken by fetch itself.  The result
     // registers are only read by that fetch.
     __device__ __forceinline__ void take_ahead() {
-        if (p.mode != kWorkStealing || cursor != 0 || has_ahead || stopped || first >= 0) return;
+        if (p.mode != kWorkStealing || solo || cursor != 0 || has_ahead || stopped || first >= 0) return;
         if (rel != 0) {
             stopped = true;
             return;
@@ -218,12 +238,15 @@ struct Scheduler {
                 const int t = first;
                 first = -1;
                 if (t < size_home) return wg.tile(home, t);
+                if (solo) return -1;  // every other ticket is some other worker's launch tile
                 cursor = 1;  // an implied ticket past the group's size: every ticket of it is taken
                 if (rel != 0) {  // and stealing takes atomics, which a release forbids
                     stopped = true;
                     return -1;
                 }
                 read_release();
+            } else if (solo) {
+                return -1;
             } else if (has_ahead) {
                 has_ahead = false;
                 const int ticket = ahead + homed(home);
@@ -291,7 +314,7 @@ struct Scheduler {
     // that finished before it, so the last one resets counters no other worker still uses;
     // the next launch (a later kernel) sees the zeros.
     __device__ __forceinline__ void finish() {
-        if (p.mode != kWorkStealing) return;
+        if (p.mode != kWorkStealing || solo) return;  // (T <= P: no counter was touched)
         const int prev = atom_add_acq_rel_gpu(p.done, 1);
         if (prev == p.workers - 1) {
             for (int g = 0; g < p.ws_groups; ++g) st_relaxed_gpu(p.counters + g * kCounterStride, 0);

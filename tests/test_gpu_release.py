@@ -22,10 +22,10 @@ def ctx():
     c.close()
 
 
-def implied_first_tile(T, G, layout, w):
-    """The tile a work-stealing worker is given at launch: ticket w div G of its home group
-    w mod G (none when the group has fewer tickets)."""
-    tiles = S.ws_group_tiles(T, G, layout)[w % G]
+def implied_first_tile(T, G, layout, w, P):
+    """The tile a work-stealing worker of P is given at launch: ticket w div G of its home
+    group w mod G (none when the group has fewer tickets)."""
+    tiles = S.ws_group_tiles(T, G, layout, P)[w % G]
     return tiles[w // G: w // G + 1]
 
 
@@ -41,7 +41,7 @@ def test_schedule_log_release_from_start(ctx):
     S.check_ws_trace([[t for (t, _, _, _) in v] for v in visits], grid.tiles, G)
     for c, v in enumerate(visits):
         if c % G in (1, 2):  # released before launch: only the tile assigned at launch
-            assert [t for (t, _, _, _) in v] == implied_first_tile(grid.tiles, G, S.WS_RANGES, c), c
+            assert [t for (t, _, _, _) in v] == implied_first_tile(grid.tiles, G, S.WS_RANGES, c, P), c
 
 
 @pytest.mark.parametrize("cfg", [pgt.CFG_1CTA_128x256, pgt.CFG_2CTA_256x256])
@@ -67,7 +67,7 @@ def test_gemm_release_from_start_same_bits(ctx, cfg):
     S.check_ws_trace([[t for (t, _, _, _) in v] for v in wv], plan["tiles"], 8)
     for w, v in enumerate(wv):
         if w % 8 != 0:  # released before launch: only the tile assigned at launch
-            assert [t for (t, _, _, _) in v] == implied_first_tile(plan["tiles"], 8, S.WS_RANGES, w), w
+            assert [t for (t, _, _, _) in v] == implied_first_tile(plan["tiles"], 8, S.WS_RANGES, w, plan["workers"]), w
 
 
 def test_gemm_release_mid_launch_from_another_stream(ctx):

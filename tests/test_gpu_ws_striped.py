@@ -58,7 +58,7 @@ def test_release_from_start(ctx):
     S.check_ws_trace([[t for (t, _, _, _) in v] for v in visits], grid.tiles, G, S.WS_STRIPED)
     for c, v in enumerate(visits):
         if c % G in (1, 2):  # released before launch: only ticket c div G of the home group
-            tiles = S.ws_group_tiles(grid.tiles, G, S.WS_STRIPED)[c % G]
+            tiles = S.ws_group_tiles(grid.tiles, G, S.WS_STRIPED, P)[c % G]
             assert [t for (t, _, _, _) in v] == tiles[c // G: c // G + 1], c
 
 

@@ -144,32 +144,59 @@ def test_ragged_last_swizzle_group_is_a_bijection():
 
 # -------------------------------------------------------------------------- work stealing
 def test_ws_partition_covers_tiles():
-    for T, G in itertools.product(range(0, 50), (1, 2, 3, 8)):
-        part = S.ws_partition(T, G)
+    for T, G, P in itertools.product(range(0, 50), (1, 2, 3, 8), (1, 3, 8, 9, 76)):
+        G = min(G, P)
+        part = S.ws_partition(T, G, P)
         ids = [t for (s, n) in part for t in range(s, s + n)]
         assert ids == list(range(T))
-        sizes = [n for (_, n) in part]
-        assert max(sizes) - min(sizes) <= 1
+        # each group's share is within one tile of T times its part of the workers
+        for (_, n), h in zip(part, S.ws_homed(P, G)):
+            assert abs(n * P - T * h) < P
+
+
+def test_ws_homed_counts_workers_by_residue():
+    assert S.ws_homed(76, 8) == [10, 10, 10, 10, 9, 9, 9, 9]
+    assert S.ws_homed(4, 3) == [2, 1, 1]
+    assert S.ws_homed(8, 8) == [1] * 8
 
 
 def test_ws_group_tiles_hand_evaluated():
-    # T = 10 tiles on 3 counters: ranges split at floor(g*10/3) = 0, 3, 6, 10; stripes take
-    # every third tile starting at the group's index
-    assert S.ws_group_tiles(10, 3, S.WS_RANGES) == [[0, 1, 2], [3, 4, 5], [6, 7, 8, 9]]
-    assert S.ws_group_tiles(10, 3, S.WS_STRIPED) == [[0, 3, 6, 9], [1, 4, 7], [2, 5, 8]]
+    # T = 10 tiles on 3 counters and 3 or 6 workers (one or two homed per group): ranges
+    # split at floor(g*10/3) = 0, 3, 6, 10; stripes take every third tile from the group's
+    # index
+    for P in (3, 6):
+        assert S.ws_group_tiles(10, 3, S.WS_RANGES, P) == [[0, 1, 2], [3, 4, 5], [6, 7, 8, 9]]
+        assert S.ws_group_tiles(10, 3, S.WS_STRIPED, P) == [[0, 3, 6, 9], [1, 4, 7], [2, 5, 8]]
+    # 4 workers: homes 0, 1, 2, 0, so group 0 has two of them.  Ranges: the workers before
+    # each group number 0, 2, 3, 4 and the bounds are floor(10*S/4) = 0, 5, 7, 10.  Stripes:
+    # tile t goes with worker t mod 4, whose home is (t mod 4) mod 3
+    assert S.ws_group_tiles(10, 3, S.WS_RANGES, 4) == [[0, 1, 2, 3, 4], [5, 6], [7, 8, 9]]
+    assert S.ws_group_tiles(10, 3, S.WS_STRIPED, 4) == [[0, 3, 4, 7, 8], [1, 5, 9], [2, 6]]
     with pytest.raises(ValueError):
-        S.ws_group_tiles(10, 3, 2)
+        S.ws_group_tiles(10, 3, 2, 3)
 
 
 @pytest.mark.parametrize("layout", [S.WS_RANGES, S.WS_STRIPED])
 def test_ws_group_tiles_partition_exactly_once(layout):
-    for T, G in itertools.product(range(0, 60), (1, 2, 3, 7, 8, 16)):
-        groups = S.ws_group_tiles(T, G, layout)
+    for T, G, P in itertools.product(range(0, 60), (1, 2, 3, 7, 8, 16), (16, 19, 76)):
+        groups = S.ws_group_tiles(T, G, layout, P)
         assert len(groups) == G
         assert sorted(t for g in groups for t in g) == list(range(T))
-        sizes = [len(g) for g in groups]
-        assert max(sizes) - min(sizes) <= 1
+        for g, h in zip(groups, S.ws_homed(P, G)):
+            assert abs(len(g) * P - T * h) < P * (1 if layout == S.WS_RANGES else 2)
         assert all(g == sorted(g) for g in groups)  # tickets follow tile order
+        if P % G == 0:  # the even split of the page's GPU, whatever the worker count
+            assert groups == S.ws_group_tiles(T, G, layout, G)
+
+
+def test_ws_balanced_when_tiles_are_a_multiple_of_workers():
+    """T = k P: every group holds exactly k tiles per home worker, in both layouts, so with
+    the launch tickets and equal progress no worker needs to steal."""
+    for P, G, k in itertools.product((76, 152, 19), (1, 4, 8, 16), (1, 4, 13)):
+        G = min(G, P)
+        for layout in (S.WS_RANGES, S.WS_STRIPED):
+            sizes = [len(g) for g in S.ws_group_tiles(k * P, G, layout, P)]
+            assert sizes == [k * h for h in S.ws_homed(P, G)]
 
 
 def test_ws_striped_first_wave_is_the_static_first_wave():
@@ -258,7 +285,7 @@ def test_ws_implied_first_random_interleavings_valid(layout, seed):
     visits = S.ws_simulate(T, P, G, lambda live: rnd.choice(live), layout=layout, implied_first=True)
     S.check_ws_trace(visits, T, G, layout)
     for c, v in enumerate(visits):  # each worker's first tile is its launch ticket, when it has one
-        tiles = S.ws_group_tiles(T, G, layout)[c % G]
+        tiles = S.ws_group_tiles(T, G, layout, P)[c % G]
         if c // G < len(tiles):
             assert v[0] == tiles[c // G]
 
@@ -282,7 +309,7 @@ def test_ws_implied_first_release_from_start_keeps_the_launch_tile():
     S.check_ws_trace(visits, T, G)
     for c, v in enumerate(visits):
         if c % G in (1, 2):
-            assert v == S.ws_group_tiles(T, G, S.WS_RANGES)[c % G][c // G: c // G + 1]
+            assert v == S.ws_group_tiles(T, G, S.WS_RANGES, P)[c % G][c // G: c // G + 1]
 
 
 def test_ws_implied_first_without_the_counter_offset_is_rejected():
@@ -373,7 +400,7 @@ def test_ws_checker_rejects_planted_mistakes(plant):
         visits[c][0], visits[c][1] = visits[c][1], visits[c][0]
     elif plant == "back":
         # worker 0 (home group 0) visiting a group-2 tile before a group-0 tile
-        part = S.ws_partition(60, 3)
+        part = S.ws_partition(60, 3, 6)
         t_g2 = part[2][0]
         for v in visits:
             if t_g2 in v:
