@@ -55,8 +55,6 @@ constexpr int kTileRing = 4;            // tile-id ring depth
 constexpr int kEpiWarps = 4;
 constexpr int kEpiBufBytes = 32 * 128;  // 32 rows x 64 bf16, 128B-swizzled, per buffer
 constexpr int kMaxSmem = 232448;        // 227 KB dynamic shared memory per CTA
-constexpr int kTicketLead = 4;          // work stealing: stages before a tile's last load that the
-                                        // next ticket is taken
 
 constexpr int pow2_at_least(int v) {
     int p = 32;
@@ -229,7 +227,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 prefetch_tensormap(&tmSFB);
             }
             const bool clc = gp.sp.mode == kLaunchControl;
-            const int lead_k = gp.k_iters > kTicketLead ? gp.k_iters - kTicketLead : 0;
             bool clc_first = true, clc_pending = false;
             uint32_t clc_phase = 0;
             // launch control: the worker's own tile first, then tiles of clusters it cancels
@@ -336,9 +333,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load<CS>(sa + L::SFB_OFF, &tmSFB, fb, 0, kg * gp.sfb_rows + n * L::NB128);
                         }
                     }
-                    // work stealing: the next tile's ticket, kTicketLead stages early (its value
-                    // is first read by the next fetch)
-                    if (leader && k == lead_k) sch.take_ahead();
                 }
             }
             if (leader) sch.finish();

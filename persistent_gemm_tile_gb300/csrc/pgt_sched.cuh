@@ -125,12 +125,13 @@ struct WsGroups {
 // Per-worker scheduler.  Static modes are pure functions of (worker, iteration); work
 // stealing draws tickets from the counters.
 //
-// Work stealing hides the protocol's round trips from the tile pipeline:
+// Work stealing keeps the protocol's round trips off the tile pipeline:
 //  * a worker's first ticket of its home group is implied: worker w, homed on g = w mod G,
 //    takes ticket w div G at launch, and the counter of g hands out tickets from n_g (the
 //    number of workers homed on g) on, so counters still start every launch at zero;
-//  * the next home ticket is taken a few pipeline stages before it is needed (take_ahead),
-//    together with reads of the following groups' counters for a steal scan;
+//  * later tickets are taken when the producer asks for the next tile, after the current
+//    tile's last load: the stages already loaded cover the atomic's round trip (taking it
+//    a few stages earlier measured slower on every shape tried);
 //  * the home group's release flag is read one decision ahead and its value used at the
 //    next one, so no decision waits for it.  A worker released before launch still runs
 //    its implied first tile; a release raised later lands within a tile;
@@ -146,22 +147,17 @@ struct Scheduler {
     int home;    // work stealing: home group
     int cursor;  // work stealing: groups found exhausted, counted from home
     int first;   // work stealing: the implied first ticket of the home group (-1 once used)
-    int ahead;   // work stealing: a home-group counter value taken before the fetch that uses it
-    bool has_ahead;
     bool stopped;  // work stealing: the home group's release flag was seen
     int rel;       // work stealing: the release flag as last read (used at the next decision)
     WsGroups wg;   // work stealing: the groups' tiles
     bool solo;     // work stealing: T <= P, every ticket implied (no counter is touched)
     static constexpr int kScan = 8;  // counters read at once by a steal scan
-    int scan[kScan];                 // work stealing: the following groups' counters, read with `ahead`
 
     __device__ __forceinline__ void init(const SchedParams& params, int worker) {
         p = params;
         home = 0;
         cursor = 0;
         first = -1;
-        ahead = 0;
-        has_ahead = false;
         stopped = false;
         rel = 0;
         solo = false;
@@ -204,27 +200,6 @@ struct Scheduler {
         rel = (p.release != nullptr && home != 0) ? *reinterpret_cast<const volatile int*>(p.release + home) : 0;
     }
 
-    // Work stealing: take the home group's next ticket now, so that the atomic's round trip
-    // overlaps other work (the producer calls this a few stages before a tile's last load);
-    // the next fetch consumes it.  A raised release flag stops the worker instead, and a
-    // ticket taken is always used, so every tile is still handed out exactly once.  Once the
-    // home group is exhausted (stealing), tickets are taken by fetch itself.  The result
-    // registers are only read by that fetch.
-    __device__ __forceinline__ void take_ahead() {
-        if (p.mode != kWorkStealing || solo || cursor != 0 || has_ahead || stopped || first >= 0) return;
-        if (rel != 0) {
-            stopped = true;
-            return;
-        }
-        ahead = atomicAdd(p.counters + home * kCounterStride, 1);
-        has_ahead = true;
-        // should the home group turn out exhausted, the steal scan starts from these reads
-        // (issued together with the atomic, so the fetch saves a round trip)
-#pragma unroll
-        for (int j = 0; j < kScan; ++j) scan[j] = read_counter(1 + j);
-        read_release();
-    }
-
     // Next tile id, or -1 when this worker is done.
     __device__ __forceinline__ int fetch() {
         if (p.mode == kWorkStealing) {
@@ -233,7 +208,6 @@ struct Scheduler {
             // exhausted: the steal scan reads up to kScan counters at once (independent loads)
             // and takes an atomic ticket only where one may be left.
             const int size_home = wg.size(home);
-            bool pre = false;  // the first steal scan may use the counters read ahead
             if (first >= 0) {
                 const int t = first;
                 first = -1;
@@ -247,12 +221,6 @@ struct Scheduler {
                 read_release();
             } else if (solo) {
                 return -1;
-            } else if (has_ahead) {
-                has_ahead = false;
-                const int ticket = ahead + homed(home);
-                if (ticket < size_home) return wg.tile(home, ticket);
-                cursor = 1;
-                pre = true;
             } else {
                 if (stopped || rel != 0) {
                     stopped = true;
@@ -266,13 +234,11 @@ struct Scheduler {
                 }
             }
             while (cursor < p.ws_groups) {
-                // A value read earlier that already reaches the group's size means exhausted;
-                // one below it is only a hint (the atomic decides), so reads taken ahead serve
-                // as well as fresh ones.
+                // A value that already reaches the group's size means exhausted; one below it
+                // is only a hint (the atomic decides).
                 int seen[kScan];
 #pragma unroll
-                for (int j = 0; j < kScan; ++j) seen[j] = pre ? scan[j] : read_counter(cursor + j);
-                pre = false;
+                for (int j = 0; j < kScan; ++j) seen[j] = read_counter(cursor + j);
                 // invariant: seen[j] belongs to the group `cursor` points at in step j
 #pragma unroll
                 for (int j = 0; j < kScan; ++j) {
