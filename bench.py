@@ -107,27 +107,121 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_burst": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
 
 
+class NvmlClockReader:
+    """Read-only NVML queries through ctypes (libnvidia-ml ships with the driver): the SM
+    clock, its maximum and the active clock-event reasons of one device.  Nothing is set."""
+
+    SM = 1  # NVML_CLOCK_SM
+    # nvmlClocksEventReasons bits (NVML's public header)
+    BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+            0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index: int, pci_bus_id: str | None = None):
+        import ctypes
+        self.ct = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        rc = 1
+        if pci_bus_id:
+            rc = lib.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(self.h))
+        if rc != 0:
+            rc = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device_index), ctypes.byref(self.h))
+        if rc != 0:
+            raise OSError("no NVML handle for the device")
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = reasons if reasons is not None else lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.max_mhz = self._clock(lib.nvmlDeviceGetMaxClockInfo)
+
+    def _clock(self, fn):
+        v = self.ct.c_uint(0)
+        return float(v.value) if fn(self.h, self.SM, self.ct.byref(v)) == 0 else None
+
+    def sample(self):
+        """(SM MHz, max SM MHz, set of active reasons), or None if a query failed."""
+        sm = self._clock(self.lib.nvmlDeviceGetClockInfo)
+        bits = self.ct.c_ulonglong(0)
+        if sm is None or self.reasons_fn(self.h, self.ct.byref(bits)) != 0:
+            return None
+        return sm, self.max_mhz, {n for b, n in self.BITS.items() if bits.value & b}
+
+
+def summarize_clocks(rows, t_begin, t_end, period_ms, source):
+    """rows: (host time, SM MHz, max MHz, active reasons).  The figures describe the samples
+    taken between t_begin and t_end (the timed launches); *_around describe all of them."""
+    inside = [r for r in rows if r[0] is not None and t_begin is not None and t_end is not None
+              and t_begin <= r[0] <= t_end]
+
+    def summary(rs):
+        return (float(np.median([r[1] for r in rs])) if rs else None,
+                sorted(set().union(*[r[3] for r in rs])) if rs else [])
+    sm_in, reasons_in = summary(inside)
+    sm_all, reasons_all = summary(rows)
+    return {"sm_mhz": sm_in, "sm_max_mhz": max((r[2] for r in rows if r[2] is not None), default=None),
+            "reasons": reasons_in, "samples": len(inside), "period_ms": period_ms, "source": source,
+            "region_s": (t_end - t_begin) if t_begin and t_end else None,
+            "sm_mhz_around": sm_all, "reasons_around": reasons_all, "samples_around": len(rows)}
+
+
 class Clocks:
-    """nvidia-smi sampling of SM clocks and throttle reasons.  Samples carry nvidia-smi's
-    timestamp; ``stop`` keeps only those taken between ``begin()`` and ``end()`` (host time
-    just before the first timed launch is enqueued and just after the last one has
-    finished), so the figures describe the timed launches.  A region shorter than the
-    sampling period may hold no sample: then ``samples`` is 0 and the figures are null,
+    """SM clocks and clock-event reasons sampled while the timed launches run.  NVML is
+    polled every millisecond from a host thread (read-only queries); without NVML,
+    nvidia-smi samples every ``period_ms``.  Samples carry host timestamps; ``stop`` keeps
+    only those taken between ``begin()`` and ``end()`` (just before the first timed launch
+    is enqueued and just after the last one has finished), so the figures describe the
+    timed launches.  A region that holds no sample reports ``samples`` 0 and null figures,
     while ``*_around`` give the samples taken around it."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    NVML_PERIOD_MS = 1
 
-    def __init__(self, device_index: int, period_ms: int = 20):
+    def __init__(self, device_index: int, period_ms: int = 20, reader=None):
         self.dev = device_index
         self.period_ms = period_ms
         self.proc = None
+        self.reader = reader
+        self.thread = None
+        self.rows = []
         self.t_begin = self.t_end = None
         self.path = os.path.join(tempfile.gettempdir(), f"pgt_clocks_{os.getpid()}.csv")
 
+    def _open_reader(self):
+        if self.reader is not None:
+            return self.reader
+        bus = None
+        try:
+            import torch
+            pr = torch.cuda.get_device_properties(self.dev)
+            if isinstance(getattr(pr, "pci_bus_id", None), int):
+                bus = f"{getattr(pr, 'pci_domain_id', 0):08x}:{pr.pci_bus_id:02x}:{getattr(pr, 'pci_device_id', 0):02x}.0"
+        except Exception:
+            bus = None
+        try:
+            return NvmlClockReader(self.dev, bus)
+        except (OSError, AttributeError):
+            return None
+
+    def _poll(self):
+        while not self.stop_flag:
+            smp = self.reader.sample()
+            if smp is not None:
+                self.rows.append((time.time(), *smp))
+            time.sleep(self.NVML_PERIOD_MS / 1000.0)
+
     def start(self):
+        self.reader = self._open_reader()
+        if self.reader is not None:
+            import threading
+            self.stop_flag = False
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            time.sleep(0.02)
+            return
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
@@ -152,8 +246,13 @@ class Clocks:
             return None
 
     def stop(self) -> dict:
+        if self.thread is not None:
+            time.sleep(0.02)
+            self.stop_flag = True
+            self.thread.join()
+            return summarize_clocks(self.rows, self.t_begin, self.t_end, self.NVML_PERIOD_MS, "nvml")
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"], "samples": 0}
         time.sleep(0.15)
         self.proc.terminate()
         self.proc.wait()
@@ -171,18 +270,7 @@ class Clocks:
                 active = {n for n, v in zip(self.REASONS, parts[6:10]) if v.lower().startswith("active")}
                 rows.append((self._parse_time(parts[0]), sm, smax, active))
         os.unlink(self.path)
-        inside = [r for r in rows if r[0] is not None and self.t_begin is not None and self.t_end is not None
-                  and self.t_begin <= r[0] <= self.t_end]
-
-        def summary(rs):
-            return (float(np.median([r[1] for r in rs])) if rs else None,
-                    sorted(set().union(*[r[3] for r in rs])) if rs else [])
-        sm_in, reasons_in = summary(inside)
-        sm_all, reasons_all = summary(rows)
-        return {"sm_mhz": sm_in, "sm_max_mhz": max((r[2] for r in rows), default=None), "reasons": reasons_in,
-                "samples": len(inside), "period_ms": self.period_ms,
-                "region_s": (self.t_end - self.t_begin) if self.t_begin and self.t_end else None,
-                "sm_mhz_around": sm_all, "reasons_around": reasons_all, "samples_around": len(rows)}
+        return summarize_clocks(rows, self.t_begin, self.t_end, self.period_ms, "nvidia-smi")
 
 
 def dist_setup(args):
