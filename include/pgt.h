@@ -78,8 +78,8 @@ extern "C" {
  *                      tile is ticket p div G of its home group, assigned at launch (a
  *                      group's counter then hands out tickets from its number of home
  *                      workers on, and still starts each launch at zero); later tickets
- *                      are taken when the worker asks for its next tile, after the current
- *                      tile's last load.
+ *                      are taken by a thread of the worker beside its loading thread, a few
+ *                      pipeline stages before the next tile is needed.
  *                      With T <= P every ticket is assigned at launch and no counter is
  *                      touched.  P at most 65535 (PGT_ERR_ARG otherwise).
  *   BLOCKED_GROUPED_M: blocked order with the L2-grouping decode, bands of group_size

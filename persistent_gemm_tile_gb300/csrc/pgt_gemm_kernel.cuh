@@ -55,6 +55,8 @@ constexpr int kTileRing = 4;            // tile-id ring depth
 constexpr int kEpiWarps = 4;
 constexpr int kEpiBufBytes = 32 * 128;  // 32 rows x 64 bf16, 128B-swizzled, per buffer
 constexpr int kMaxSmem = 232448;        // 227 KB dynamic shared memory per CTA
+constexpr int kTicketLead = 8;          // work stealing: the next tile is asked for this many
+                                        // stages before the current tile's last load
 
 constexpr int pow2_at_least(int v) {
     int p = 32;
@@ -95,10 +97,11 @@ struct Layout {
     static constexpr int EPI_BUFS = (STAGES * STAGE_BYTES + kEpiWarps * 2 * kEpiBufBytes + 2048 <= kMaxSmem) ? 2 : 1;
     static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
     static constexpr int BAR_OFF = EPI_OFF + kEpiWarps * EPI_BUFS * kEpiBufBytes;
-    // barriers: full[S], empty[S], tfull[2], tempty[2], sfull[Q], sempty[Q], mma_done, clc
-    static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * kTileRing + 2;
+    // barriers: full[S], empty[S], tfull[2], tempty[2], sfull[Q], sempty[Q], mma_done, clc,
+    // ticket request, ticket ready
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * kTileRing + 4;
     static constexpr int RING_OFF = BAR_OFF + (NUM_BARS * 8 + 15) / 16 * 16;  // int4 entries
-    static constexpr int MISC_OFF = RING_OFF + kTileRing * 16;                // tmem slot, abort flag
+    static constexpr int MISC_OFF = RING_OFF + kTileRing * 16;                // tmem slot, abort flag, ticket
     static constexpr int CLC_OFF = MISC_OFF + 16;                             // launch-control answer
     static constexpr int BYTES = CLC_OFF + 16;
     static constexpr int SMEM = BYTES + 1024;  // alignment slack
@@ -164,10 +167,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = rank == 0;
     const int worker = blockIdx.x / CS;
 
-    // The producer thread of the worker (the leader CTA's thread 0) runs the scheduler.
-    // Work stealing starts reading its release flag here, so the read overlaps the set-up.
+    // The scheduler runs on one thread of the worker's leader CTA: the producer (thread 0) for
+    // the static orders, the ticket thread (warp 2, lane 0) for work stealing, whose counter
+    // round trips then never sit in the producer's instruction stream.  Work stealing starts
+    // reading its release flag here, so the read overlaps the set-up.
+    const bool ws = gp.sp.mode == kWorkStealing;
     Scheduler sch;
-    if (threadIdx.x == 0 && leader) sch.init(gp.sp, worker);
+    if (leader && threadIdx.x == (ws ? 64 : 0)) sch.init(gp.sp, worker);
 
     const uint32_t bar0 = base + L::BAR_OFF;
     auto full = [&](int s) { return bar0 + 8u * s; };
@@ -178,6 +184,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto sempty = [&](int q) { return bar0 + 8u * (2 * STAGES + 4 + kTileRing + q); };
     const uint32_t mma_done = bar0 + 8u * (2 * STAGES + 4 + 2 * kTileRing);
     const uint32_t clc_bar = mma_done + 8u;
+    const uint32_t tk_req = clc_bar + 8u;  // work stealing: the producer asks for its next tile
+    const uint32_t tk_rdy = clc_bar + 16u;  // work stealing: the ticket thread has answered
+    volatile int* tk_val = reinterpret_cast<volatile int*>(gbase + L::MISC_OFF + 8);
     const uint32_t clc_resp = base + L::CLC_OFF;
     int4* ring = reinterpret_cast<int4*>(gbase + L::RING_OFF);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + L::MISC_OFF);
@@ -200,6 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(mma_done, 1);
         mbar_init(clc_bar, 1);
+        mbar_init(tk_req, 1);
+        mbar_init(tk_rdy, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -227,6 +238,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 prefetch_tensormap(&tmSFB);
             }
             const bool clc = gp.sp.mode == kLaunchControl;
+            // work stealing: the ticket thread fetches the next tile while this one loads
+            const int lead_k = gp.k_iters > kTicketLead ? gp.k_iters - kTicketLead : 0;
+            uint32_t tk_phase = 0;
+            auto ws_next = [&]() -> int {
+                if (!mbar_wait(tk_rdy, tk_phase & 1u, abort_flag, gp.err, kRoleProducer, 12)) return -1;
+                ++tk_phase;
+                return *tk_val;
+            };
+            if (ws && leader) mbar_arrive(tk_req);  // the first tile: its launch ticket
             bool clc_first = true, clc_pending = false;
             uint32_t clc_phase = 0;
             // launch control: the worker's own tile first, then tiles of clusters it cancels
@@ -259,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int q = qc % kTileRing;
                 const uint32_t qpar = (qc / kTileRing) & 1u;
                 if (leader) {
-                    t = *abort_flag ? -1 : (clc ? clc_fetch() : sch.fetch());
+                    t = *abort_flag ? -1 : (clc ? clc_fetch() : (ws ? ws_next() : sch.fetch()));
                     if (t >= 0) decode_tile(gp.sp, t, m, n);
                     if (!mbar_wait<kPair>(sempty(q), qpar ^ 1u, abort_flag, gp.err, kRoleProducer, 0)) break;
                     ring[q] = make_int4(t, m, n, 0);
@@ -333,9 +353,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load<CS>(sa + L::SFB_OFF, &tmSFB, fb, 0, kg * gp.sfb_rows + n * L::NB128);
                         }
                     }
+                    if (ws && leader && k == lead_k) mbar_arrive(tk_req);  // ask for the next tile
                 }
             }
-            if (leader) sch.finish();
             if (clc_pending) {
                 // never leave with an answer still to land in this CTA's shared memory
                 volatile int no_abort = 0;
@@ -422,6 +442,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(mma_done);
             volatile int no_abort = 0;
             mbar_wait(mma_done, 0, &no_abort, gp.err, kRoleMma, 5);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // -------------------------------------------------- work-stealing tickets
+        // One answer per request: the producer asks for its next tile a few stages before
+        // the current tile's last load; this thread takes the ticket (counter round trips
+        // included) and hands the tile id over through shared memory.
+        if (ws && leader && lane == 0) {
+            uint32_t ph = 0;
+            for (;;) {
+                if (!mbar_wait(tk_req, ph & 1u, abort_flag, gp.err, kRoleScheduler, 13)) break;
+                ++ph;
+                const int t = *abort_flag ? -1 : sch.fetch();
+                *tk_val = t;
+                mbar_arrive(tk_rdy);
+                if (t < 0) break;
+            }
+            sch.finish();
         }
         __syncwarp();
     } else if (warp >= 4) {

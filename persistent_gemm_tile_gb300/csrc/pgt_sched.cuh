@@ -129,9 +129,10 @@ struct WsGroups {
 //  * a worker's first ticket of its home group is implied: worker w, homed on g = w mod G,
 //    takes ticket w div G at launch, and the counter of g hands out tickets from n_g (the
 //    number of workers homed on g) on, so counters still start every launch at zero;
-//  * later tickets are taken when the producer asks for the next tile, after the current
-//    tile's last load: the stages already loaded cover the atomic's round trip (taking it
-//    a few stages earlier measured slower on every shape tried);
+//  * later tickets are taken by a thread of their own (the GEMM kernel's ticket thread), a
+//    few stages before the producer needs the next tile, so the counter round trips never
+//    sit in the producer's instruction stream (an early ticket taken by the producer itself
+//    measured slower than a late one);
 //  * the home group's release flag is read one decision ahead and its value used at the
 //    next one, so no decision waits for it.  A worker released before launch still runs
 //    its implied first tile; a release raised later lands within a tile;
