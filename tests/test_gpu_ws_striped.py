@@ -113,3 +113,17 @@ def test_unknown_layout_rejected(ctx):
         ctx.schedule_log(4, 4, 1, pgt.WORK_STEALING, 1, 2, 4, tb.struct, ws_layout=2)
     assert e.value.status == pgt.ERR_ARG
 
+
+
+def test_worker_limit_for_work_stealing(ctx):
+    """Work stealing's group arithmetic is 32-bit for P <= 65535: more workers are refused on
+    the host before anything is launched (other modes are not limited)."""
+    tb = pgt.TraceBuffers(1, 1)
+    with pytest.raises(pgt.PgtError) as e:
+        ctx.schedule_log(4, 4, 1, pgt.WORK_STEALING, 1, 2, 65536, tb.struct)
+    assert e.value.status == pgt.ERR_ARG
+    A = torch.zeros((64, 64), dtype=torch.int16, device="cuda")
+    desc = pgt.make_desc(64, 64, 64, sched_mode=pgt.WORK_STEALING, num_workers=65536)
+    with pytest.raises(pgt.PgtError) as e:
+        ctx.gemm_ex(desc, A, A, A)
+    assert e.value.status == pgt.ERR_ARG
