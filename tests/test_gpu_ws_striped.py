@@ -127,3 +127,33 @@ def test_worker_limit_for_work_stealing(ctx):
     with pytest.raises(pgt.PgtError) as e:
         ctx.gemm_ex(desc, A, A, A)
     assert e.value.status == pgt.ERR_ARG
+
+
+@pytest.mark.parametrize("layout", [pgt.WS_RANGES, pgt.WS_STRIPED])
+@pytest.mark.parametrize("K", [64, 576, 2048])
+def test_uneven_home_counts_and_short_tiles(ctx, layout, K):
+    """7 workers on 3 counter groups (homes 3, 2, 2: shares in proportion), with K from one
+    stage (the next tile asked for at the tile's first load) to many: exact-once visits in
+    each worker's order, the launch tiles, and the static order's bits."""
+    M, N = 1280, 1536
+    A, B = synthetic.gemm_bf16_inputs(M, N, K, seed=93)
+    dA, dB = dev_u16(A), dev_u16(B)
+    ref = torch.empty((M, N), dtype=torch.int16, device="cuda")
+    ctx.gemm_ex(pgt.make_desc(M, N, K, sched_mode=pgt.SWIZZLED, kernel_cfg=pgt.CFG_1CTA_128x128), dA, dB, ref)
+    desc = pgt.make_desc(M, N, K, sched_mode=pgt.WORK_STEALING, ws_groups=3, ws_layout=layout, num_workers=7,
+                         kernel_cfg=pgt.CFG_1CTA_128x128)
+    plan = ctx.gemm_plan(desc)
+    assert plan["workers"] == 7 and plan["ws_groups"] == 3
+    for _ in range(2):  # the second launch relies on the in-kernel counter reset
+        tb = pgt.TraceBuffers(plan["ctas"], plan["tiles"])
+        C = torch.full((M, N), -1, dtype=torch.int16, device="cuda")
+        ctx.gemm_ex(desc, dA, dB, C, trace=tb.struct)
+        torch.cuda.synchronize()
+        assert ctx.last_error()[0] == 0
+        assert torch.equal(C, ref)
+        visits, _ = tb.read()
+        lists = [[t for (t, _, _, _) in v] for v in visits]
+        S.check_ws_trace(lists, plan["tiles"], 3, layout)
+        groups = S.ws_group_tiles(plan["tiles"], 3, layout, 7)
+        for w, v in enumerate(lists):
+            assert v[0] == groups[w % 3][w // 3]  # the launch ticket
