@@ -169,11 +169,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // The scheduler runs on one thread of the worker's leader CTA: the producer (thread 0) for
     // the static orders, the ticket thread (warp 2, lane 0) for work stealing, whose counter
-    // round trips then never sit in the producer's instruction stream.  Work stealing starts
-    // reading its release flag here, so the read overlaps the set-up.
+    // round trips then never sit in the producer's instruction stream.  (With work stealing
+    // the producer keeps a copy only to take its launch tile at once; the ticket thread then
+    // drops that ticket.)  Work stealing starts reading its release flag here, so the read
+    // overlaps the set-up.
     const bool ws = gp.sp.mode == kWorkStealing;
     Scheduler sch;
-    if (leader && threadIdx.x == (ws ? 64 : 0)) sch.init(gp.sp, worker);
+    if (leader && (threadIdx.x == 0 || (ws && threadIdx.x == 64))) sch.init(gp.sp, worker);
 
     const uint32_t bar0 = base + L::BAR_OFF;
     auto full = [&](int s) { return bar0 + 8u * s; };
@@ -241,12 +243,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             // work stealing: the ticket thread fetches the next tile while this one loads
             const int lead_k = gp.k_iters > kTicketLead ? gp.k_iters - kTicketLead : 0;
             uint32_t tk_phase = 0;
+            int ws_first = (ws && leader) ? sch.launch_tile() : -1;  // taken without a round trip
+            // with no more tiles than workers every ticket is a launch ticket: nothing to ask for
+            const bool ws_ask = ws && leader && !sch.solo;
             auto ws_next = [&]() -> int {
+                if (ws_first >= 0) {
+                    const int t = ws_first;
+                    ws_first = -1;
+                    return t;
+                }
+                if (!ws_ask) return -1;
                 if (!mbar_wait(tk_rdy, tk_phase & 1u, abort_flag, gp.err, kRoleProducer, 12)) return -1;
                 ++tk_phase;
                 return *tk_val;
             };
-            if (ws && leader) mbar_arrive(tk_req);  // the first tile: its launch ticket
+            // no launch tile (its home group has too few tickets): ask the ticket thread at once
+            if (ws_ask && ws_first < 0) mbar_arrive(tk_req);
             bool clc_first = true, clc_pending = false;
             uint32_t clc_phase = 0;
             // launch control: the worker's own tile first, then tiles of clusters it cancels
@@ -353,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load<CS>(sa + L::SFB_OFF, &tmSFB, fb, 0, kg * gp.sfb_rows + n * L::NB128);
                         }
                     }
-                    if (ws && leader && k == lead_k) mbar_arrive(tk_req);  // ask for the next tile
+                    if (ws_ask && k == lead_k) mbar_arrive(tk_req);  // ask for the next tile
                 }
             }
             if (clc_pending) {
@@ -452,7 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // One answer per request: the producer asks for its next tile a few stages before
         // the current tile's last load; this thread takes the ticket (counter round trips
         // included) and hands the tile id over through shared memory.
-        if (ws && leader && lane == 0) {
+        if (ws && leader && lane == 0 && !sch.solo) {
+            sch.drop_launch_ticket();  // the producer has taken it
             uint32_t ph = 0;
             for (;;) {
                 if (!mbar_wait(tk_req, ph & 1u, abort_flag, gp.err, kRoleScheduler, 13)) break;

@@ -183,6 +183,17 @@ struct Scheduler {
         }
     }
 
+    // Work stealing: the tile of this worker's launch ticket, or -1 when its home group holds
+    // no such ticket (the worker then starts by stealing).  No side effect: a second thread
+    // of the worker may run the scheduler and drop the ticket (drop_launch_ticket) after the
+    // first has taken the tile itself.
+    __device__ __forceinline__ int launch_tile() const {
+        return (p.mode == kWorkStealing && first >= 0 && first < wg.size(home)) ? wg.tile(home, first) : -1;
+    }
+    __device__ __forceinline__ void drop_launch_ticket() {
+        if (launch_tile() >= 0) first = -1;
+    }
+
     // Work stealing: workers homed on group g (G <= P, so at least one): the implied tickets
     // 0 .. n_g - 1 of g belong to them, and the counter's value c stands for ticket c + n_g.
     __device__ __forceinline__ int homed(int g) const { return wg.homed(g); }
