@@ -57,6 +57,8 @@ constexpr int kEpiBufBytes = 32 * 128;  // 32 rows x 64 bf16, 128B-swizzled, per
 constexpr int kMaxSmem = 232448;        // 227 KB dynamic shared memory per CTA
 constexpr int kTicketLead = 8;          // work stealing: the next tile is asked for this many
                                         // stages before the current tile's last load
+constexpr int kSchedPatience = 8;       // bounded waits the scheduler thread may chain for a
+                                        // free ring entry while every other role progresses
 
 constexpr int pow2_at_least(int v) {
     int p = 32;
@@ -98,10 +100,10 @@ struct Layout {
     static constexpr int EPI_OFF = STAGES * STAGE_BYTES;
     static constexpr int BAR_OFF = EPI_OFF + kEpiWarps * EPI_BUFS * kEpiBufBytes;
     // barriers: full[S], empty[S], tfull[2], tempty[2], sfull[Q], sempty[Q], mma_done, clc,
-    // ticket request, ticket ready
-    static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * kTileRing + 4;
+    // ticket request
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + 2 * kTileRing + 3;
     static constexpr int RING_OFF = BAR_OFF + (NUM_BARS * 8 + 15) / 16 * 16;  // int4 entries
-    static constexpr int MISC_OFF = RING_OFF + kTileRing * 16;                // tmem slot, abort flag, ticket
+    static constexpr int MISC_OFF = RING_OFF + kTileRing * 16;                // tmem slot, abort flag
     static constexpr int CLC_OFF = MISC_OFF + 16;                             // launch-control answer
     static constexpr int BYTES = CLC_OFF + 16;
     static constexpr int SMEM = BYTES + 1024;  // alignment slack
@@ -167,15 +169,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = rank == 0;
     const int worker = blockIdx.x / CS;
 
-    // The scheduler runs on one thread of the worker's leader CTA: the producer (thread 0) for
-    // the static orders, the ticket thread (warp 2, lane 0) for work stealing, whose counter
-    // round trips then never sit in the producer's instruction stream.  (With work stealing
-    // the producer keeps a copy only to take its launch tile at once; the ticket thread then
-    // drops that ticket.)  Work stealing starts reading its release flag here, so the read
-    // overlaps the set-up.
+    // The scheduler runs on a thread of its own in the worker's leader CTA (warp 2, lane 0)
+    // and posts each decision into the tile ring ahead of the roles that read it, so no
+    // decision (a decode, a counter round trip, the writes into the pair's other CTA) sits
+    // in the producer's instruction stream at a tile boundary.  The static orders run up to
+    // a ring's depth ahead; work stealing takes each later ticket only when the producer
+    // asks for it, a few stages before its current tile's last load.  Launch control stays
+    // in the producer, which cancels a cluster once it has taken a tile.  Work stealing
+    // starts reading its release flag here, so the read overlaps the set-up.
     const bool ws = gp.sp.mode == kWorkStealing;
+    const bool clc = gp.sp.mode == kLaunchControl;
+    const bool sched_thread = !clc;  // the ring is written by warp 2 (else by the producer)
     Scheduler sch;
-    if (leader && (threadIdx.x == 0 || (ws && threadIdx.x == 64))) sch.init(gp.sp, worker);
+    if (leader && sched_thread && threadIdx.x == 64) sch.init(gp.sp, worker);
 
     const uint32_t bar0 = base + L::BAR_OFF;
     auto full = [&](int s) { return bar0 + 8u * s; };
@@ -187,8 +193,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t mma_done = bar0 + 8u * (2 * STAGES + 4 + 2 * kTileRing);
     const uint32_t clc_bar = mma_done + 8u;
     const uint32_t tk_req = clc_bar + 8u;  // work stealing: the producer asks for its next tile
-    const uint32_t tk_rdy = clc_bar + 16u;  // work stealing: the ticket thread has answered
-    volatile int* tk_val = reinterpret_cast<volatile int*>(gbase + L::MISC_OFF + 8);
     const uint32_t clc_resp = base + L::CLC_OFF;
     int4* ring = reinterpret_cast<int4*>(gbase + L::RING_OFF);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + L::MISC_OFF);
@@ -205,14 +209,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int q = 0; q < kTileRing; ++q) {
             mbar_init(sfull(q), 1);
-            // consumers of a ring entry: the MMA thread, the epilogue warps, and in a pair
-            // also the peer's producer and epilogue warps (all counted on the leader)
-            mbar_init(sempty(q), kPair ? 2 + 2 * kEpiWarps : 1 + kEpiWarps);
+            // consumers of a ring entry: the MMA thread, the epilogue warps, in a pair also the
+            // peer's producer and epilogue warps (all counted on the leader), and this CTA's
+            // producer when the scheduler thread writes the ring
+            mbar_init(sempty(q), (kPair ? 2 + 2 * kEpiWarps : 1 + kEpiWarps) + (sched_thread ? 1 : 0));
         }
         mbar_init(mma_done, 1);
         mbar_init(clc_bar, 1);
         mbar_init(tk_req, 1);
-        mbar_init(tk_rdy, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -230,6 +234,48 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (TRACE && threadIdx.x == 0 && gp.tr_times != nullptr) gp.tr_times[2 * blockIdx.x] = (int64_t)globaltimer();
 
+    // K direction of a tile (bf16): tiles of alternate waves walk K backwards, so a wave starts
+    // on the K slices of the panels the previous wave read last, which are still in L2.  A
+    // tile's wave is its position in the 16-column-group order (the swizzled order with group
+    // 16) divided by kdir_period, the number of workers the GPU holds at once.  It depends on
+    // (m, n) alone, so each output tile has one K order whatever the scheduler, group size or
+    // worker count.
+    auto k_reversed = [&](int m, int n) -> bool {
+        if (MX || gp.kdir_period <= 0) return false;
+        const int g16 = min(16, gp.sp.n_tiles);
+        const int grp = n / g16;
+        const int gw = min(g16, gp.sp.n_tiles - grp * g16);
+        const int pos = grp * g16 * gp.sp.m_tiles + m * gw + (n - grp * g16);
+        return ((pos / gp.kdir_period) & 1) != 0;
+    };
+    // Post tile t (-1: no more tiles) as ring entry qc for every role of the worker, decoded
+    // and with its K direction, in this CTA and, in a pair, in the other CTA as well.  The
+    // scheduler thread runs up to a ring's depth ahead of the slowest reader (the epilogue),
+    // so its wait for a free entry may span more than a tile: it keeps waiting, one bounded
+    // wait after another, while no other role has given up (at most kSchedPatience rounds).
+    auto post_tile = [&](uint32_t qc, int t, int role, int site, bool patient) -> bool {
+        const int q = qc % kTileRing;
+        const uint32_t par = ((qc / kTileRing) & 1u) ^ 1u;
+        int m = 0, n = 0, rev = 0;
+        if (t >= 0) {
+            decode_tile(gp.sp, t, m, n);
+            rev = k_reversed(m, n) ? 1 : 0;
+        }
+        bool got = false;
+        for (int r = 0; patient && !got && r < kSchedPatience && !*abort_flag; ++r) {
+            volatile int quiet = 0;  // a round that runs out reports nothing
+            got = mbar_wait<kPair>(sempty(q), par, &quiet, nullptr, role, site);
+        }
+        if (!got && !mbar_wait<kPair>(sempty(q), par, abort_flag, gp.err, role, site)) return false;
+        ring[q] = make_int4(t, m, n, rev);
+        if constexpr (kPair) {
+            st_shared_cluster_v4(mapa_shared(smem_u32(ring + q), 1), t, m, n, rev);
+            mbar_arrive_remote(mapa_shared(sfull(q), 1));
+        }
+        mbar_arrive(sfull(q));
+        return true;
+    };
+
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
@@ -239,26 +285,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 prefetch_tensormap(&tmSFA);
                 prefetch_tensormap(&tmSFB);
             }
-            const bool clc = gp.sp.mode == kLaunchControl;
-            // work stealing: the ticket thread fetches the next tile while this one loads
+            // work stealing: the scheduler thread takes the next ticket when asked, this many
+            // stages before the current tile's last load; with no more tiles than workers
+            // every ticket is a launch ticket and there is nothing to ask for
             const int lead_k = gp.k_iters > kTicketLead ? gp.k_iters - kTicketLead : 0;
-            uint32_t tk_phase = 0;
-            int ws_first = (ws && leader) ? sch.launch_tile() : -1;  // taken without a round trip
-            // with no more tiles than workers every ticket is a launch ticket: nothing to ask for
-            const bool ws_ask = ws && leader && !sch.solo;
-            auto ws_next = [&]() -> int {
-                if (ws_first >= 0) {
-                    const int t = ws_first;
-                    ws_first = -1;
-                    return t;
-                }
-                if (!ws_ask) return -1;
-                if (!mbar_wait(tk_rdy, tk_phase & 1u, abort_flag, gp.err, kRoleProducer, 12)) return -1;
-                ++tk_phase;
-                return *tk_val;
-            };
-            // no launch tile (its home group has too few tickets): ask the ticket thread at once
-            if (ws_ask && ws_first < 0) mbar_arrive(tk_req);
+            const bool ws_ask = ws && leader && gp.sp.tiles > gp.sp.workers;
             bool clc_first = true, clc_pending = false;
             uint32_t clc_phase = 0;
             // launch control: the worker's own tile first, then tiles of clusters it cancels
@@ -287,29 +318,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             int nvis = 0;
             bool ok = true;
             while (ok) {
-                int t, m = 0, n = 0;
                 const int q = qc % kTileRing;
-                const uint32_t qpar = (qc / kTileRing) & 1u;
-                if (leader) {
-                    t = *abort_flag ? -1 : (clc ? clc_fetch() : (ws ? ws_next() : sch.fetch()));
-                    if (t >= 0) decode_tile(gp.sp, t, m, n);
-                    if (!mbar_wait<kPair>(sempty(q), qpar ^ 1u, abort_flag, gp.err, kRoleProducer, 0)) break;
-                    ring[q] = make_int4(t, m, n, 0);
-                    if constexpr (kPair) {
-                        const uint32_t ring_addr = smem_u32(ring + q);
-                        st_shared_cluster_v4(mapa_shared(ring_addr, 1), t, m, n, 0);
-                        mbar_arrive_remote(mapa_shared(sfull(q), 1));
-                    }
-                    mbar_arrive(sfull(q));
+                if (leader && !sched_thread) {
+                    // launch control: this thread takes the tile and writes the ring itself
+                    if (!post_tile(qc, *abort_flag ? -1 : clc_fetch(), kRoleProducer, 0, false)) break;
                 } else {
-                    if (!mbar_wait<true>(sfull(q), qpar, abort_flag, gp.err, kRoleProducer, 8)) break;
-                    const int4 e = ring[q];
-                    t = e.x;
-                    m = e.y;
-                    n = e.z;
-                    mbar_arrive_remote(mapa_shared(sempty(q), 0));
+                    // read the entry the scheduler thread (or, for the pair's other CTA, the
+                    // leader) posted, then hand the entry back
+                    if (!mbar_wait<kPair>(sfull(q), (qc / kTileRing) & 1u, abort_flag, gp.err, kRoleProducer, 8)) break;
                 }
+                const int4 e = ring[q];
+                if (sched_thread || !leader) arrive_local_or_leader(sempty(q), !leader);
                 ++qc;
+                const int t = e.x, m = e.y, n = e.z;
+                const bool rev = e.w != 0;
                 if (t < 0) break;
                 if (TRACE && gp.tr_visits != nullptr) {
                     if (nvis < gp.tr_max) {
@@ -323,20 +345,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const int row0 = (m * CS + (int)rank) * L::BM;  // this CTA's rows of A
                 const int col0 = n * BN + (int)rank * L::BN_CTA;  // this CTA's slice of B
-                // K direction: tiles of alternate waves walk K backwards, so a wave starts on the
-                // K slices of the panels the previous wave read last, which are still in L2.
-                // A tile's wave is its position in the 16-column-group order (the swizzled
-                // order with group 16) divided by kdir_period, the number of workers the GPU
-                // holds at once.  It depends on (m, n) alone, so each output tile has one K
-                // order whatever the scheduler, group size or worker count.
-                bool rev = false;
-                if (!MX && gp.kdir_period > 0) {
-                    const int g16 = min(16, gp.sp.n_tiles);
-                    const int grp = n / g16;
-                    const int gw = min(g16, gp.sp.n_tiles - grp * g16);
-                    const int pos = grp * g16 * gp.sp.m_tiles + m * gw + (n - grp * g16);
-                    rev = ((pos / gp.kdir_period) & 1) != 0;
-                }
                 for (int k = 0; k < gp.k_iters; ++k, ++it) {
                     const int kc = rev ? gp.k_iters - 1 - k : k;  // K slice loaded at iteration k
                     const int s = it % STAGES;
@@ -460,22 +468,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else if (warp == 2) {
-        // -------------------------------------------------- work-stealing tickets
-        // One answer per request: the producer asks for its next tile a few stages before
-        // the current tile's last load; this thread takes the ticket (counter round trips
-        // included) and hands the tile id over through shared memory.
-        if (ws && leader && lane == 0 && !sch.solo) {
-            sch.drop_launch_ticket();  // the producer has taken it
-            uint32_t ph = 0;
+        // ---------------------------------------------------------- scheduler
+        // Posts the worker's tiles into the ring.  Static orders: as fast as entries free up.
+        // Work stealing: the launch ticket at once (no counter round trip), every later
+        // ticket when the producer asks for it; then the last worker resets the counters.
+        if (leader && lane == 0 && sched_thread) {
+            uint32_t qc = 0, ph = 0;
             for (;;) {
-                if (!mbar_wait(tk_req, ph & 1u, abort_flag, gp.err, kRoleScheduler, 13)) break;
-                ++ph;
+                if (ws && qc > 0 && !sch.solo) {
+                    if (!mbar_wait(tk_req, ph & 1u, abort_flag, gp.err, kRoleScheduler, 13)) break;
+                    ++ph;
+                }
                 const int t = *abort_flag ? -1 : sch.fetch();
-                *tk_val = t;
-                mbar_arrive(tk_rdy);
+                if (!post_tile(qc, t, kRoleScheduler, 11, true)) break;
+                ++qc;
                 if (t < 0) break;
             }
-            sch.finish();
+            if (ws) sch.finish();
         }
         __syncwarp();
     } else if (warp >= 4) {

@@ -129,7 +129,7 @@ struct WsGroups {
 //  * a worker's first ticket of its home group is implied: worker w, homed on g = w mod G,
 //    takes ticket w div G at launch, and the counter of g hands out tickets from n_g (the
 //    number of workers homed on g) on, so counters still start every launch at zero;
-//  * later tickets are taken by a thread of their own (the GEMM kernel's ticket thread), a
+//  * later tickets are taken by a thread of their own (the GEMM kernel's scheduler thread), a
 //    few stages before the producer needs the next tile, so the counter round trips never
 //    sit in the producer's instruction stream (an early ticket taken by the producer itself
 //    measured slower than a late one);
