@@ -81,6 +81,16 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
                  : "memory");
 }
 
+// The same without release semantics.  A cluster-scope release makes the arriving thread
+// wait until its earlier memory operations are visible to the whole cluster (measured: over
+// a thousand cycles); this form is for arrivals whose ordering is already settled, e.g. a
+// hand-back of tensor memory whose loads were waited for, or an arrival issued after the
+// loaded value it releases has been consumed by an earlier instruction.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(

@@ -149,6 +149,14 @@ __device__ __forceinline__ void arrive_local_or_leader(uint32_t local_bar, bool 
         mbar_arrive(local_bar);
 }
 
+// The same for an arrival that needs no release: the pair's other CTA then arrives relaxed.
+__device__ __forceinline__ void arrive_local_or_leader_relaxed(uint32_t local_bar, bool remote) {
+    if (remote)
+        mbar_arrive_remote_relaxed(mapa_shared(local_bar, 0));
+    else
+        mbar_arrive(local_bar);
+}
+
 template <int CS, int BN, int STAGES, bool B_MN, bool MX, bool TRACE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -328,11 +336,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!mbar_wait<kPair>(sfull(q), (qc / kTileRing) & 1u, abort_flag, gp.err, kRoleProducer, 8)) break;
                 }
                 const int4 e = ring[q];
-                if (sched_thread || !leader) arrive_local_or_leader(sempty(q), !leader);
+                // The leader hands the entry back at once (a CTA-scope arrive).  The pair's
+                // other CTA does so after the tile's first loads, whose coordinates consume
+                // the entry, so its arrive can be relaxed (a cluster-scope release would hold
+                // up those loads).
+                if (sched_thread && leader) mbar_arrive(sempty(q));
+                bool held = !leader;
                 ++qc;
                 const int t = e.x, m = e.y, n = e.z;
                 const bool rev = e.w != 0;
-                if (t < 0) break;
+                if (t < 0) {
+                    if (held) mbar_arrive_remote_relaxed(mapa_shared(sempty(q), 0));
+                    break;
+                }
                 if (TRACE && gp.tr_visits != nullptr) {
                     if (nvis < gp.tr_max) {
                         int32_t* r = gp.tr_visits + ((int64_t)blockIdx.x * gp.tr_max + nvis) * PGT_VISIT_FIELDS;
@@ -373,8 +389,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load<CS>(sa + L::SFB_OFF, &tmSFB, fb, 0, kg * gp.sfb_rows + n * L::NB128);
                         }
                     }
+                    if (held) {
+                        mbar_arrive_remote_relaxed(mapa_shared(sempty(q), 0));
+                        held = false;
+                    }
                     if (ws_ask && k == lead_k) mbar_arrive(tk_req);  // ask for the next tile
                 }
+                if (held) mbar_arrive_remote_relaxed(mapa_shared(sempty(q), 0));  // no load issued
             }
             if (clc_pending) {
                 // never leave with an answer still to land in this CTA's shared memory
@@ -579,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) arrive_local_or_leader(tempty(acc), !leader);
+                if (lane == 0) arrive_local_or_leader_relaxed(tempty(acc), !leader);
 #pragma unroll
                 for (int c = 0; c < BN / 64; ++c) store_chunk(c, pk + 32 * c);
             } else {
@@ -595,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // accumulator fully read: hand it back to the MMA warp
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) arrive_local_or_leader(tempty(acc), !leader);
+                        if (lane == 0) arrive_local_or_leader_relaxed(tempty(acc), !leader);
                     }
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -621,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_wait();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) arrive_local_or_leader(tempty(acc), !leader);
+                    if (lane == 0) arrive_local_or_leader_relaxed(tempty(acc), !leader);
                     auto tv = [&](int i) __attribute__((always_inline)) -> uint32_t {
                         if constexpr (kTail == 16)
                             return tb[i];
