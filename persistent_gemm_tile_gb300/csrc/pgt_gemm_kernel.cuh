@@ -566,30 +566,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             if constexpr (L::ACC_BUFS == 1) {
                 // a single accumulator: read all of it into registers (as bf16 pairs), hand
-                // it back to the MMA warp at once, then stage and store
-                // pk[j] holds columns 2j and 2j + 1; the accumulator is read 128 columns per
-                // wait, so the MMA warp gets it back after two load round trips
+                // it back to the MMA warp at once, then stage and store.  pk[j] holds columns
+                // 2j and 2j + 1; the accumulator is read 128 columns per wait, and handed back
+                // as soon as the last load has landed, before its columns are converted
                 static_assert(BN % 128 == 0, "single-accumulator tiles are read 128 columns at a time");
                 uint32_t pk[BN / 2];
-                if (!gp.epi) {
 #pragma unroll
-                    for (int h = 0; h < BN / 128; ++h) {
-                        uint32_t r[4][32];
+                for (int h = 0; h < BN / 128; ++h) {
+                    uint32_t r[4][32];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) tmem_ld_32x32b_x32(tacc + h * 128 + 32 * q, r[q]);
-                        tmem_ld_wait();
+                    for (int q = 0; q < 4; ++q) tmem_ld_32x32b_x32(tacc + h * 128 + 32 * q, r[q]);
+                    tmem_ld_wait();
+                    if (h == BN / 128 - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) arrive_local_or_leader_relaxed(tempty(acc), !leader);
+                    }
+                    if (!gp.epi) {
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
 #pragma unroll
                             for (int i = 0; i < 16; ++i) pk[64 * h + 16 * q + i] = pack_bf16x2(r[q][2 * i], r[q][2 * i + 1]);
-                    }
-                } else {
-#pragma unroll
-                    for (int h = 0; h < BN / 128; ++h) {
-                        uint32_t r[4][32];
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) tmem_ld_32x32b_x32(tacc + h * 128 + 32 * q, r[q]);
-                        tmem_ld_wait();
+                    } else {
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
 #pragma unroll
@@ -598,9 +596,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     cvt(r[q][2 * i], r[q][2 * i + 1], col0 + 128 * h + 32 * q + 2 * i);
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) arrive_local_or_leader_relaxed(tempty(acc), !leader);
 #pragma unroll
                 for (int c = 0; c < BN / 64; ++c) store_chunk(c, pk + 32 * c);
             } else {
