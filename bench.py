@@ -41,12 +41,12 @@ L2_NOTE = "inputs larger than L2: A+B+C = 384 MiB per GEMM > 129 MB L2; add x+y+
 GEMM_SOURCES = ["csrc/pgt_gemm_kernel.cuh", "csrc/pgt_device.cuh", "csrc/pgt_sched.cuh"]
 ADD_SOURCES = ["csrc/pgt_add.cu", "csrc/pgt_device.cuh", "csrc/pgt_sched.cuh"]
 PROFILED_TRAFFIC = {
-    "gemm_bf16_2cta_256x256": (8.65503488e+08 + 1.26967552e+08, GEMM_SOURCES, "fa4138744bbc2e3c"),
-    "gemm_mxfp8_2cta_256x256": (2.45559040e+08 + 1.16458496e+08, GEMM_SOURCES, "fa4138744bbc2e3c"),
-    "add_wide_8x1024_blocked": (5.36938496e+08 + 2.31415296e+08, ADD_SOURCES, "1163f5f012df5edf"),
-    "add_wide_8x1024_interleaved": (5.36943872e+08 + 2.31419648e+08, ADD_SOURCES, "1163f5f012df5edf"),
-    "add_page_32x16_blocked": (5.36942336e+08 + 2.33105664e+08, ADD_SOURCES, "1163f5f012df5edf"),
-    "add_page_32x16_interleaved": (5.61978880e+08 + 2.38232576e+08, ADD_SOURCES, "1163f5f012df5edf"),
+    "gemm_bf16_2cta_256x256": (8.72220928e+08 + 1.27668992e+08, GEMM_SOURCES, "3544384e1d189e1b"),
+    "gemm_mxfp8_2cta_256x256": (2.49933056e+08 + 1.16242688e+08, GEMM_SOURCES, "3544384e1d189e1b"),
+    "add_wide_8x1024_blocked": (5.36941568e+08 + 2.31527936e+08, ADD_SOURCES, "ee0be5eebefbc724"),
+    "add_wide_8x1024_interleaved": (5.36939264e+08 + 2.31156480e+08, ADD_SOURCES, "ee0be5eebefbc724"),
+    "add_page_32x16_blocked": (5.36938496e+08 + 2.33322752e+08, ADD_SOURCES, "ee0be5eebefbc724"),
+    "add_page_32x16_interleaved": (5.64816640e+08 + 2.38495744e+08, ADD_SOURCES, "ee0be5eebefbc724"),
 }
 
 
