@@ -91,6 +91,24 @@ __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar)
                  : "memory");
 }
 
+// Arm a barrier of another CTA of the cluster: one arrival plus `bytes` expected through
+// complete_tx, without release semantics (the bytes bring their own, below).
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote_relaxed(uint32_t cluster_bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_bar),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Asynchronous 16-byte store into another CTA's shared memory; its completion is counted on
+// that CTA's barrier (complete_tx, release at cluster scope), so a thread that sees the
+// barrier's phase complete sees the data, and the storing thread does not wait.
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, int a, int b, int c, int d, uint32_t cluster_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.s32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     cluster_addr),
+                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -153,12 +171,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                      : "memory");
-}
-
-__device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr, int a, int b, int c, int d) {
-    asm volatile("st.shared::cluster.v4.s32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
-                 "r"(c), "r"(d)
-                 : "memory");
 }
 
 // ------------------------------------------------------- cluster launch control

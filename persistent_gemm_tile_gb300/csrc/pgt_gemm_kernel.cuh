@@ -277,8 +277,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!got && !mbar_wait<kPair>(sempty(q), par, abort_flag, gp.err, role, site)) return false;
         ring[q] = make_int4(t, m, n, rev);
         if constexpr (kPair) {
-            st_shared_cluster_v4(mapa_shared(smem_u32(ring + q), 1), t, m, n, rev);
-            mbar_arrive_remote(mapa_shared(sfull(q), 1));
+            // the other CTA's copy: an asynchronous store whose 16 bytes that CTA's barrier
+            // counts, armed by a relaxed arrive (a cluster-scope release arrive would hold
+            // this thread up for about a microsecond)
+            const uint32_t peer_full = mapa_shared(sfull(q), 1);
+            mbar_arrive_expect_tx_remote_relaxed(peer_full, 16);
+            st_async_v4(mapa_shared(smem_u32(ring + q), 1), t, m, n, rev, peer_full);
         }
         mbar_arrive(sfull(q));
         return true;
