@@ -41,12 +41,12 @@ L2_NOTE = "inputs larger than L2: A+B+C = 384 MiB per GEMM > 129 MB L2; add x+y+
 GEMM_SOURCES = ["csrc/pgt_gemm_kernel.cuh", "csrc/pgt_device.cuh", "csrc/pgt_sched.cuh"]
 ADD_SOURCES = ["csrc/pgt_add.cu", "csrc/pgt_device.cuh", "csrc/pgt_sched.cuh"]
 PROFILED_TRAFFIC = {
-    "gemm_bf16_2cta_256x256": (8.72220928e+08 + 1.27668992e+08, GEMM_SOURCES, "3544384e1d189e1b"),
-    "gemm_mxfp8_2cta_256x256": (2.49933056e+08 + 1.16242688e+08, GEMM_SOURCES, "3544384e1d189e1b"),
-    "add_wide_8x1024_blocked": (5.36941568e+08 + 2.31527936e+08, ADD_SOURCES, "ee0be5eebefbc724"),
-    "add_wide_8x1024_interleaved": (5.36939264e+08 + 2.31156480e+08, ADD_SOURCES, "ee0be5eebefbc724"),
-    "add_page_32x16_blocked": (5.36938496e+08 + 2.33322752e+08, ADD_SOURCES, "ee0be5eebefbc724"),
-    "add_page_32x16_interleaved": (5.64816640e+08 + 2.38495744e+08, ADD_SOURCES, "ee0be5eebefbc724"),
+    "gemm_bf16_2cta_256x256": (8.66333440e+08 + 1.27151360e+08, GEMM_SOURCES, "f175484a1e0015c6"),
+    "gemm_mxfp8_2cta_256x256": (2.47468288e+08 + 1.15645952e+08, GEMM_SOURCES, "f175484a1e0015c6"),
+    "add_wide_8x1024_blocked": (5.36939520e+08 + 2.31422720e+08, ADD_SOURCES, "4144b88cceddf147"),
+    "add_wide_8x1024_interleaved": (5.36960768e+08 + 2.30933504e+08, ADD_SOURCES, "4144b88cceddf147"),
+    "add_page_32x16_blocked": (5.36942848e+08 + 2.33459456e+08, ADD_SOURCES, "4144b88cceddf147"),
+    "add_page_32x16_interleaved": (5.66916352e+08 + 2.37809920e+08, ADD_SOURCES, "4144b88cceddf147"),
 }
 
 
