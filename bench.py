@@ -37,29 +37,40 @@ L2_NOTE = "inputs larger than L2: A+B+C = 384 MiB per GEMM > 129 MB L2; add x+y+
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture
 # of each kernel (summaries under profiles/).  A figure is reported only while the kernel's
-# sources hash to the fingerprint taken with it; after any change the roofline says null.
+# sources hash to the fingerprint taken with it (comments and blank lines left out, so an
+# edit of comments alone keeps a capture); after any change of code the roofline says null.
 GEMM_SOURCES = ["csrc/pgt_gemm_kernel.cuh", "csrc/pgt_device.cuh", "csrc/pgt_sched.cuh"]
 ADD_SOURCES = ["csrc/pgt_add.cu", "csrc/pgt_device.cuh", "csrc/pgt_sched.cuh"]
 PROFILED_TRAFFIC = {
-    "gemm_bf16_2cta_256x256": (8.66333440e+08 + 1.27151360e+08, GEMM_SOURCES, "f175484a1e0015c6"),
-    "gemm_mxfp8_2cta_256x256": (2.47468288e+08 + 1.15645952e+08, GEMM_SOURCES, "f175484a1e0015c6"),
-    "add_wide_8x1024_blocked": (5.36939520e+08 + 2.31422720e+08, ADD_SOURCES, "4144b88cceddf147"),
-    "add_wide_8x1024_interleaved": (5.36960768e+08 + 2.30933504e+08, ADD_SOURCES, "4144b88cceddf147"),
-    "add_page_32x16_blocked": (5.36942848e+08 + 2.33459456e+08, ADD_SOURCES, "4144b88cceddf147"),
-    "add_page_32x16_interleaved": (5.66916352e+08 + 2.37809920e+08, ADD_SOURCES, "4144b88cceddf147"),
+    "gemm_bf16_2cta_256x256": (8.66333440e+08 + 1.27151360e+08, GEMM_SOURCES, "95db09673622310a"),
+    "gemm_mxfp8_2cta_256x256": (2.47468288e+08 + 1.15645952e+08, GEMM_SOURCES, "95db09673622310a"),
+    "add_wide_8x1024_blocked": (5.36939520e+08 + 2.31422720e+08, ADD_SOURCES, "ea072a4ea074ca89"),
+    "add_wide_8x1024_interleaved": (5.36960768e+08 + 2.30933504e+08, ADD_SOURCES, "ea072a4ea074ca89"),
+    "add_page_32x16_blocked": (5.36942848e+08 + 2.33459456e+08, ADD_SOURCES, "ea072a4ea074ca89"),
+    "add_page_32x16_interleaved": (5.66916352e+08 + 2.37809920e+08, ADD_SOURCES, "ea072a4ea074ca89"),
 }
 
 
-def profiled_traffic(key: str):
+def source_fingerprint(files) -> str:
+    """First 16 hex digits of the sha256 of the kernel sources' code: every line up to a `//`
+    comment, trailing blanks removed, empty lines dropped (the sources use no block
+    comments and no `//` inside strings)."""
     import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "persistent_gemm_tile_gb300", f), encoding="utf-8") as fh:
+            for line in fh:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(key: str):
     if key not in PROFILED_TRAFFIC:
         return None
     nbytes, files, fingerprint = PROFILED_TRAFFIC[key]
-    h = hashlib.sha256()
-    for f in files:
-        with open(os.path.join(ROOT, "persistent_gemm_tile_gb300", f), "rb") as fh:
-            h.update(fh.read())
-    return nbytes if h.hexdigest()[:16] == fingerprint else None
+    return nbytes if source_fingerprint(files) == fingerprint else None
 
 
 def parse():

@@ -1,8 +1,8 @@
 // Device code of the persistent tiled GEMM (the host side is pgt_gemm.cu).
 //
 // Persistent tiled GEMM C = A . B for sm_103a: TMA producer warp, tcgen05 MMA warp issuing
-// into tensor-memory accumulators, four epilogue warps, an mbarrier stage ring, and a
-// tile-id ring that carries the scheduler's choices to every role.
+// into tensor-memory accumulators, a scheduler thread, four epilogue warps, an mbarrier
+// stage ring, and a tile-id ring that carries the scheduler's choices to every role.
 //
 // Design source: the warp-specialised persistent kernel of "[Feature] Introduce tile
 // scheduler" (tilelang PR #2441, gemm_mxfp8_blockscaled_1d1d.py): TMA warp, MMA warp,
@@ -12,10 +12,11 @@
 // pair owns tile row bx = m_idx * 2 + cta_id and loads half of B's tile, and MXFP8 scales
 // (one E8M0 byte per row and 128-wide K block) copied to tensor memory for block-scaled
 // MMAs.  Differences: the accumulator is double buffered whenever tensor memory allows, so
-// the epilogue of one tile overlaps the next tile's mainloop; the producer runs the
-// scheduler and publishes each tile through a small shared-memory ring (needed for work
-// stealing, where roles cannot recompute the tile); scales are repacked once per call into
-// the tensor-memory copy layout, so no transpose warp is needed.
+// the epilogue of one tile overlaps the next tile's mainloop; a scheduler thread of its own
+// publishes each tile ahead through a small shared-memory ring (needed for work stealing,
+// where roles cannot recompute the tile, and keeping every decision out of the producer's
+// instruction stream); scales are repacked once per call into the tensor-memory copy
+// layout, so no transpose warp is needed.
 //
 // Template parameters: CS = CTAs per worker (1, or 2 for a cluster pair issuing
 // cta_group::2 MMAs with M = 256); BN = output columns per worker tile; B_MN = B stored
@@ -50,7 +51,7 @@ struct GemmParams {
     int64_t* tr_times;
 };
 
-constexpr int kThreads = 256;           // warp 0 producer, warp 1 MMA, warps 4-7 epilogue
+constexpr int kThreads = 256;           // warp 0 producer, warp 1 MMA, warp 2 scheduler, warps 4-7 epilogue
 constexpr int kTileRing = 4;            // tile-id ring depth
 constexpr int kEpiWarps = 4;
 constexpr int kEpiBufBytes = 32 * 128;  // 32 rows x 64 bf16, 128B-swizzled, per buffer
