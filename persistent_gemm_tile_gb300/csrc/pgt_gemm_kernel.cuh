@@ -427,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 tc_fence_after();
                 const uint32_t d = tmem_base + acc * L::ACC_STRIDE;
-                // two stages per loop body: this single thread's issue loop is on the tensor
-                // pipe's critical path (MXFP8: 5-7% faster than one stage per body, measured)
+                // two stages per loop body (MXFP8: 5-7% faster than one stage per body,
+                // measured): this single thread runs only about a stage ahead of the pipe
 #pragma unroll 2
                 for (int k = 0; k < gp.k_iters; ++k, ++it) {
                     const int s = it % STAGES;
